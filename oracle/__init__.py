@@ -1,0 +1,176 @@
+"""CPU oracle for the BitNet b1.58 W2A8 path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The CUDA
+library never imports it and shares no code with it.
+
+This module is argument marshalling (numpy arrays in, numpy arrays out) around
+``bitnet_oracle.c``; every step of the arithmetic is in that C file, which
+cites the passage of the pages each function follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+_i64 = ctypes.c_int64
+_f32 = ctypes.c_float
+_p = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    from .build import build_oracle
+
+    return build_oracle(force=force)
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH) or _stale():
+        build()
+    lib = ctypes.CDLL(_LIB_PATH)
+    sig = {
+        "oracle_bf16_to_f32": (None, [_p, _i64, _p]),
+        "oracle_abs_sum": (ctypes.c_double, [_p, _i64]),
+        "oracle_absmean": (_f32, [_p, _i64]),
+        "oracle_gamma": (_f32, [_f32, _f32, _f32]),
+        "oracle_ternarize": (ctypes.c_int, [_f32, _f32]),
+        "oracle_pack_codes": (None, [_p, _i64, _p]),
+        "oracle_unpack_codes": (None, [_p, _i64, _p]),
+        "oracle_pack_weights": (None, [_p, _i64, _i64, _f32, _f32, _p, _p, _p]),
+        "oracle_quant_act": (None, [_p, _i64, _i64, _p, _p]),
+        "oracle_contract": (None, [_p, _p, _i64, _i64, _i64, _i64, _i64, _p]),
+        "oracle_epilogue": (None, [_p, _p, _f32, _i64, _i64, _p]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _stale() -> bool:
+    src = os.path.join(_HERE, "bitnet_oracle.c")
+    return os.path.getmtime(src) > os.path.getmtime(_LIB_PATH)
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, dtype=np.float32)
+    _load().oracle_bf16_to_f32(_ptr(bits), bits.size, _ptr(out))
+    return out
+
+
+def abs_sum(w: np.ndarray) -> float:
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    return _load().oracle_abs_sum(_ptr(w), w.size)
+
+
+def absmean(w: np.ndarray) -> np.float32:
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    return np.float32(_load().oracle_absmean(_ptr(w), w.size))
+
+
+def gamma(mean: float, alpha: float = 1.0, eps: float = 1e-8) -> np.float32:
+    return np.float32(_load().oracle_gamma(mean, alpha, eps))
+
+
+def ternarize(g: float, w: float) -> int:
+    return int(_load().oracle_ternarize(g, w))
+
+
+def pack_codes(q: np.ndarray) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.int8).ravel()
+    out = np.empty((q.size + 3) // 4, dtype=np.uint8)
+    _load().oracle_pack_codes(_ptr(q), q.size, _ptr(out))
+    return out
+
+
+def unpack_codes(packed: np.ndarray, n: int) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8).ravel()
+    assert packed.size * 4 >= n
+    out = np.empty(n, dtype=np.int8)
+    _load().oracle_unpack_codes(_ptr(packed), n, _ptr(out))
+    return out
+
+
+def pack_weights(W: np.ndarray, alpha: float = 1.0, eps: float = 1e-8):
+    """Returns (packed uint8 [ceil(N*K/4)], beta float32, absmean float32)."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    assert W.ndim == 2
+    N, K = W.shape
+    packed = np.empty((N * K + 3) // 4, dtype=np.uint8)
+    beta = np.zeros(1, dtype=np.float32)
+    am = np.zeros(1, dtype=np.float32)
+    _load().oracle_pack_weights(_ptr(W), N, K, alpha, eps, _ptr(packed), _ptr(beta), _ptr(am))
+    return packed, beta[0], am[0]
+
+
+def quant_act(x: np.ndarray):
+    """x fp32 [M, K] -> (x_q int8 [M, K], scale fp32 [M] = per-token absmax)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.ndim == 2
+    M, K = x.shape
+    xq = np.empty((M, K), dtype=np.int8)
+    s = np.empty(M, dtype=np.float32)
+    _load().oracle_quant_act(_ptr(x), M, K, _ptr(xq), _ptr(s))
+    return xq, s
+
+
+def contract(xq: np.ndarray, packed: np.ndarray, N: int, K: int, rows=None, threads: int = 1):
+    """int32 acc [M, N]; only rows in ``rows`` (range or None = all) are filled.
+
+    ``threads`` > 1 splits the row range over a thread pool; the C routine
+    releases the GIL, each thread computes a disjoint block of rows.
+    """
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    M = xq.shape[0]
+    assert xq.shape == (M, K) and packed.size * 4 >= N * K
+    acc = np.zeros((M, N), dtype=np.int32)
+    r0, r1 = (0, N) if rows is None else (rows[0], rows[1])
+    lib = _load()
+    if threads <= 1 or r1 - r0 < 2:
+        lib.oracle_contract(_ptr(xq), _ptr(packed), M, N, K, r0, r1, _ptr(acc))
+        return acc
+    from concurrent.futures import ThreadPoolExecutor
+
+    bounds = np.linspace(r0, r1, threads + 1).astype(np.int64)
+    with ThreadPoolExecutor(threads) as ex:
+        futs = [
+            ex.submit(lib.oracle_contract, _ptr(xq), _ptr(packed), M, N, K, int(a), int(b), _ptr(acc))
+            for a, b in zip(bounds[:-1], bounds[1:]) if b > a
+        ]
+        for f in futs:
+            f.result()
+    return acc
+
+
+def epilogue(acc: np.ndarray, scale: np.ndarray, w_scale: float) -> np.ndarray:
+    acc = np.ascontiguousarray(acc, dtype=np.int32)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    M, N = acc.shape
+    y = np.empty((M, N), dtype=np.float32)
+    _load().oracle_epilogue(_ptr(acc), _ptr(scale), w_scale, M, N, _ptr(y))
+    return y
+
+
+def bitlinear(x: np.ndarray, packed: np.ndarray, beta: float, N: int, K: int, threads: int = 1):
+    """Whole decode/prefill path: quant_act -> contraction -> epilogue."""
+    xq, s = quant_act(x)
+    acc = contract(xq, packed, N, K, threads=threads)
+    return epilogue(acc, s, beta), acc, xq, s

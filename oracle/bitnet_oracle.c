@@ -1,0 +1,189 @@
+/*
+ * bitnet_oracle.c -- plain, slow CPU oracle for the BitNet b1.58 W2A8 path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check of the
+ * package entry point and the CPU-baseline leg of the benchmark may load or
+ * call this file.  The CUDA library shares no code, header, table or helper
+ * with it, and neither side includes the other.
+ *
+ * Sources (pages on the BitNet subject; cited by title and section):
+ *   [Deep-dive]  "BitNet 深度拆解：当大模型被压到 1.58 bit——从三元权重、BitLinear
+ *                 到 bitnet.cpp 的端侧推理革命（2026）"
+ *   [devpress]   devpress.csdn.net BitNet post, section "三值量化：把乘法变成加减法"
+ *   [Hands-on]   "1-bit推理框架bitnet.cpp实测：三元权重原理与本地部署"
+ *
+ * Every floating-point step is written as the one IEEE-754 operation it names
+ * (build with -O2 -ffp-contract=off, no fast-math; x86-64 SSE arithmetic has
+ * no excess precision).  Rounding to integer is rint() in the default
+ * round-to-nearest-even mode, which is the rounding torch.round performs.
+ *
+ * Readings where the pages leave a step open (listed again in the design
+ * notes of the repository):
+ *   - mean|W| is summed in fp64 in a fixed order: chunks of 4096 consecutive
+ *     row-major elements, each summed left to right, chunk sums added left to
+ *     right; the mean is (float)(S / n).
+ *   - eps is added after alpha*mean, in fp32, as the absmean listing writes it.
+ *   - beta = mean(|W_ternary|) = nnz / n, formed in fp64 and rounded once.
+ *   - the dequantised output divides by qmax = 127 (the BitLinear forward in
+ *     [Deep-dive] section 3.1 multiplies by the raw absmax only).
+ *   - a NaN product gamma*w ternarises to 0; NaN activations are unspecified.
+ *
+ * Pins: every function below is checked against values fixed by the pages or
+ * by mathematics (worked examples, closed forms, invariants, brute force); see
+ * tests/test_oracle_pins.py.  No function here is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORACLE_ABS_CHUNK 4096
+
+/* bf16 is the upper half of an fp32 word, so widening is exact (activation
+ * dtype, [Deep-dive] section 6.5: norms etc. stay fp32, only linear inputs
+ * are quantised). */
+void oracle_bf16_to_f32(const uint16_t *in, int64_t n, float *out) {
+  for (int64_t i = 0; i < n; i++) {
+    uint32_t bits = (uint32_t)in[i] << 16;
+    memcpy(&out[i], &bits, sizeof bits);
+  }
+}
+
+/* S = sum |w_i|, fp64, fixed order (reading of weight.abs().mean() in the
+ * absmean listing, [Deep-dive] section 2.2). */
+double oracle_abs_sum(const float *w, int64_t n) {
+  double total = 0.0;
+  for (int64_t c0 = 0; c0 < n; c0 += ORACLE_ABS_CHUNK) {
+    int64_t c1 = c0 + ORACLE_ABS_CHUNK < n ? c0 + ORACLE_ABS_CHUNK : n;
+    double part = 0.0;
+    for (int64_t i = c0; i < c1; i++) part += fabs((double)w[i]);
+    total += part;
+  }
+  return total;
+}
+
+/* mean|W| rounded to fp32 (the weight tensor is fp32). */
+float oracle_absmean(const float *w, int64_t n) {
+  if (n <= 0) return 0.0f;
+  return (float)(oracle_abs_sum(w, n) / (double)n);
+}
+
+/* gamma = 1 / (alpha * mean|W| + eps), three fp32 operations in the order of
+ * the absmean listing, [Deep-dive] section 2.2. */
+float oracle_gamma(float mean, float alpha, float eps) {
+  float t = alpha * mean;
+  t = t + eps;
+  return 1.0f / t;
+}
+
+/* W_ternary = clamp(round(gamma * w), -1, 1), [Deep-dive] section 2.2. */
+int oracle_ternarize(float gamma, float w) {
+  float p = gamma * w;
+  if (isnan(p)) return 0;
+  float r = rintf(p);
+  if (r > 1.0f) r = 1.0f;
+  if (r < -1.0f) r = -1.0f;
+  return (int)r; /* -0.0 becomes 0 */
+}
+
+/* INT2 packing, [Deep-dive] section 3.3 (pack_ternary): code = w + 1 in
+ * {0,1,2}; the flattened codes are grouped four to a byte, the first in the
+ * lowest two bits; a ragged tail is padded with code 0. */
+void oracle_pack_codes(const int8_t *q, int64_t n, uint8_t *packed) {
+  int64_t nbytes = (n + 3) / 4;
+  for (int64_t j = 0; j < nbytes; j++) {
+    unsigned byte = 0;
+    for (int s = 0; s < 4; s++) {
+      int64_t i = 4 * j + s;
+      unsigned code = i < n ? (unsigned)(q[i] + 1) : 0u;
+      byte |= (code & 3u) << (2 * s);
+    }
+    packed[j] = (uint8_t)byte;
+  }
+}
+
+/* Unpacking, [Deep-dive] section 3.3 (unpack_ternary): field s of byte j is
+ * flat element 4j+s; value = code - 1 (a code 3, never produced, reads +2). */
+void oracle_unpack_codes(const uint8_t *packed, int64_t n, int8_t *q) {
+  for (int64_t i = 0; i < n; i++) {
+    int code = (packed[i / 4] >> (2 * (i % 4))) & 3;
+    q[i] = (int8_t)(code - 1);
+  }
+}
+
+/* Offline weight preparation: absmean ternarisation, 2-bit packing and the
+ * beta scale, [Deep-dive] sections 2.2, 2.3 and 3.3.  W is [N, K] row-major
+ * fp32; packed receives ceil(N*K/4) bytes. */
+void oracle_pack_weights(const float *W, int64_t N, int64_t K, float alpha, float eps,
+                         uint8_t *packed, float *beta, float *absmean) {
+  int64_t n = N * K;
+  float mean = oracle_absmean(W, n);
+  float gamma = oracle_gamma(mean, alpha, eps);
+  int64_t nnz = 0;
+  int64_t nbytes = (n + 3) / 4;
+  for (int64_t j = 0; j < nbytes; j++) {
+    int8_t q[4] = {0, 0, 0, 0};
+    int64_t cnt = n - 4 * j < 4 ? n - 4 * j : 4;
+    for (int64_t s = 0; s < cnt; s++) {
+      q[s] = (int8_t)oracle_ternarize(gamma, W[4 * j + s]);
+      if (q[s] != 0) nnz++;
+    }
+    oracle_pack_codes(q, cnt, &packed[j]);
+  }
+  *beta = (float)((double)nnz / (double)n);
+  *absmean = mean;
+}
+
+/* Per-token absmax activation quantisation, [Deep-dive] section 2.2
+ * (absmax_quantize, bits = 8): s = max(max_k |x|, 1e-8);
+ * q = clamp(round(x / s * 127), -127, 127).  Divide first, then multiply. */
+void oracle_quant_act(const float *x, int64_t M, int64_t K, int8_t *xq, float *scale) {
+  const float qmax = 127.0f;
+  for (int64_t m = 0; m < M; m++) {
+    const float *row = x + m * K;
+    float s = 0.0f;
+    for (int64_t k = 0; k < K; k++) {
+      float a = fabsf(row[k]);
+      if (a > s) s = a;
+    }
+    if (s < 1e-8f) s = 1e-8f;
+    scale[m] = s;
+    for (int64_t k = 0; k < K; k++) {
+      float v = row[k] / s;
+      v = v * qmax;
+      float r = rintf(v);
+      if (r > qmax) r = qmax;
+      if (r < -qmax) r = -qmax;
+      xq[m * K + k] = (int8_t)r;
+    }
+  }
+}
+
+/* Integer contraction acc[m, n] = sum_k W_ternary[n, k] * x_q[m, k] over the
+ * packed weights ("整数域矩阵乘", [Deep-dive] section 3.1; the -1/0/+1 product
+ * identity of section 1), for output rows n in [n_begin, n_end).  Accumulated
+ * in int64 and stored as int32 (|acc| <= 254 K). */
+void oracle_contract(const int8_t *xq, const uint8_t *packed, int64_t M, int64_t N, int64_t K,
+                     int64_t n_begin, int64_t n_end, int32_t *acc) {
+  for (int64_t n = n_begin; n < n_end; n++) {
+    for (int64_t m = 0; m < M; m++) {
+      int64_t a = 0;
+      for (int64_t k = 0; k < K; k++) {
+        int64_t i = n * K + k;
+        int w = ((packed[i / 4] >> (2 * (i % 4))) & 3) - 1;
+        a += (int64_t)w * (int64_t)xq[m * K + k];
+      }
+      acc[m * N + n] = (int32_t)a;
+    }
+  }
+}
+
+/* Dequantisation Y = acc * beta * s_m / 127 ([Deep-dive] section 2.3, with
+ * the activation scale read as absmax / qmax), computed in fp64 and rounded
+ * once to fp32. */
+void oracle_epilogue(const int32_t *acc, const float *scale, float w_scale, int64_t M, int64_t N,
+                     float *y) {
+  for (int64_t m = 0; m < M; m++)
+    for (int64_t n = 0; n < N; n++)
+      y[m * N + n] =
+          (float)((double)acc[m * N + n] * (double)w_scale * (double)scale[m] / 127.0);
+}

@@ -1,0 +1,328 @@
+"""Pins the CPU oracle to what the pages and mathematics fix (no GPU).
+
+Each test states the fact it checks.  None of them re-types the oracle's own
+formula: they use hand-derived worked examples (tests/golden), invariants,
+closed forms, exact rational arithmetic, brute force on tiny inputs, and the
+alternative formulations the pages give.
+"""
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from conftest import load_golden
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ---------------------------------------------------------------- packing ---
+
+def test_pack_worked_tuples(oracle_mod):
+    g = load_golden("pack_tuples.json")
+    for case in g["cases"]:
+        got = oracle_mod.pack_codes(np.array(case["ternary"], dtype=np.int8))
+        assert got.tolist() == case["packed"], case
+
+
+def test_pack_all_81_tuples_round_trip_and_bijection(oracle_mod):
+    # 3^4 ternary 4-tuples: each packs to one byte, unpacking returns it, the 81
+    # bytes are distinct and no 2-bit field is 3 (codes are w+1 in {0,1,2}).
+    tuples = np.array(list(itertools.product([-1, 0, 1], repeat=4)), dtype=np.int8)
+    packed = oracle_mod.pack_codes(tuples.ravel())
+    assert packed.size == 81  # four weights per byte
+    assert len(set(packed.tolist())) == 81
+    for b in packed.tolist():
+        assert all(((b >> (2 * s)) & 3) != 3 for s in range(4))
+    back = oracle_mod.unpack_codes(packed, tuples.size)
+    assert np.array_equal(back, tuples.ravel())
+
+
+def test_pack_round_trip_random_and_sizes(oracle_mod):
+    rng = np.random.default_rng(7)
+    for n in [1, 2, 3, 4, 5, 7, 8, 1023, 4096, 4097]:
+        q = rng.integers(-1, 2, size=n).astype(np.int8)
+        p = oracle_mod.pack_codes(q)
+        assert p.size == (n + 3) // 4
+        assert np.array_equal(oracle_mod.unpack_codes(p, n), q)
+        # ragged tail: padding fields hold code 0
+        if n % 4:
+            last = int(p[-1])
+            for s in range(n % 4, 4):
+                assert (last >> (2 * s)) & 3 == 0
+
+
+def test_unpack_reads_code3_as_plus2(oracle_mod):
+    # unpack_ternary subtracts 1 from the raw field; a field 3 (never produced
+    # by packing) therefore reads +2.
+    assert oracle_mod.unpack_codes(np.array([0xFF], dtype=np.uint8), 4).tolist() == [2, 2, 2, 2]
+
+
+# ---------------------------------------------------------- ternarisation ---
+
+def _check_pack_golden(oracle_mod, name):
+    g = load_golden(name)
+    W = np.array(g["W"], dtype=np.float32)
+    packed, beta, am = oracle_mod.pack_weights(W)
+    assert packed.tolist() == g["packed"]
+    assert float(beta) == g["beta"]
+    n = W.size
+    assert oracle_mod.unpack_codes(packed, n).tolist() == g["ternary"]
+    if "absmean" in g:
+        assert float(am) == g["absmean"]
+        assert float(oracle_mod.gamma(am)) == g["gamma"]
+
+
+def test_ternarize_worked_example_round_half_even_and_clamp(oracle_mod):
+    _check_pack_golden(oracle_mod, "ternarize_worked.json")
+
+
+def test_ternarize_multiplies_by_reciprocal(oracle_mod):
+    _check_pack_golden(oracle_mod, "ternarize_reciprocal.json")
+
+
+def test_ternarize_thresholds_at_half_gamma(oracle_mod):
+    # With gamma = 1 (mean|W| = 1), the code is the nearest integer clamped to
+    # [-1, 1]: |w| < 0.5 -> 0, |w| > 0.5 -> sign(w); exact halves go to 0.
+    for w, want in [(0.4999, 0), (0.5001, 1), (-0.5001, -1), (7.0, 1), (-7.0, -1), (0.0, 0),
+                    (-0.0, 0), (1e-30, 0), (np.inf, 1), (-np.inf, -1)]:
+        assert oracle_mod.ternarize(1.0, w) == want, w
+
+
+def test_absmean_equals_exact_mean_to_fp32_rounding(oracle_mod):
+    rng = np.random.default_rng(3)
+    for n in [1, 5, 4095, 4096, 4097, 20000]:
+        w = (rng.standard_normal(n) * rng.choice([1e-3, 1.0, 50.0])).astype(np.float32)
+        exact = sum(Fraction(float(abs(v))) for v in w) / n
+        got = oracle_mod.absmean(w)
+        # fp64 accumulation error is far below half an fp32 ulp, so the result
+        # is within one fp32 ulp of the exact mean (and almost always equal to
+        # the correctly rounded value).
+        ulp = np.spacing(np.float32(float(exact)))
+        assert abs(Fraction(float(got)) - exact) <= Fraction(float(ulp))
+        assert got == np.float32(float(exact)) or n > 4096
+
+
+def test_gamma_special_cases(oracle_mod):
+    # mean 1 -> gamma exactly 1 (eps vanishes in fp32); mean 0 (all-zero
+    # weights) -> gamma = 1/fl32(1e-8); alpha scales the mean.
+    assert float(oracle_mod.gamma(1.0)) == 1.0
+    assert float(oracle_mod.gamma(0.0)) == float(np.float32(1.0) / np.float32(1e-8))
+    assert float(oracle_mod.gamma(2.0, alpha=0.5)) == 1.0
+    assert float(oracle_mod.gamma(0.25)) == 4.0
+
+
+def test_all_zero_weights_give_beta_zero_and_zero_output(oracle_mod):
+    # An all-zero weight matrix (a checkpoint defect reported in the
+    # microsoft-bitnet review, section 06) must ternarise to all zeros.
+    W = np.zeros((8, 16), dtype=np.float32)
+    packed, beta, am = oracle_mod.pack_weights(W)
+    assert float(beta) == 0.0 and float(am) == 0.0
+    assert np.all(packed == 0x55)  # every code is 1 (weight 0)
+    x = np.random.default_rng(0).standard_normal((3, 16)).astype(np.float32)
+    y, acc, _, _ = oracle_mod.bitlinear(x, packed, beta, 8, 16)
+    assert np.all(acc == 0) and np.all(y == 0)
+
+
+def _phi(z):
+    return 0.5 * (1.0 + math.erf(z / math.sqrt(2.0)))
+
+
+@pytest.mark.parametrize("dist", ["gauss", "laplace"])
+def test_beta_closed_form(oracle_mod, dist):
+    # For i.i.d. W, gamma ~ 1/E|W| and P(code 0) = P(|W| < E|W|/2):
+    #   Gaussian: E|W| = sigma*sqrt(2/pi), P0 = 2*Phi(sqrt(2/pi)/2) - 1 = 0.3101
+    #   Laplace(b): E|W| = b, P0 = 1 - exp(-1/2) = 0.3935
+    # beta = 1 - P0 must hold within binomial noise (5 sigma).
+    rng = np.random.default_rng(11)
+    N, K = 1024, 2048
+    if dist == "gauss":
+        W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+        p0 = 2 * _phi(math.sqrt(2 / math.pi) / 2) - 1
+    else:
+        W = rng.laplace(0.0, 0.01, (N, K)).astype(np.float32)
+        p0 = 1 - math.exp(-0.5)
+    _, beta, _ = oracle_mod.pack_weights(W)
+    n = N * K
+    sigma = math.sqrt(p0 * (1 - p0) / n)
+    assert abs(float(beta) - (1 - p0)) < 5 * sigma + 2e-4
+
+
+# --------------------------------------------------------- quant_act ---
+
+def test_quant_act_worked_example(oracle_mod):
+    g = load_golden("quant_act_worked.json")
+    xq, s = oracle_mod.quant_act(np.array(g["x"], dtype=np.float32))
+    assert xq.tolist() == g["x_q"]
+    assert [float(v) for v in s] == [float(np.float32(v)) for v in g["scale"]]
+
+
+def _all_finite_bf16():
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    f = (bits << 16).view(np.float32)
+    return f[np.isfinite(f)]
+
+
+@pytest.mark.parametrize("smax", [1.0, 3.0, 0.0123, 1000.0])
+def test_quant_act_all_bf16_within_half_step(oracle_mod, smax):
+    # Every finite bf16 value v with |v| <= smax, placed in a row whose absmax
+    # is smax, must quantise to the integer nearest 127*v/smax (the exact real
+    # value), up to the fp32 rounding of the two operations (< 4e-5), with
+    # the row maximum mapping to exactly 127.
+    v = _all_finite_bf16()
+    v = v[np.abs(v) <= smax]
+    x = np.zeros((v.size, 2), dtype=np.float32)
+    x[:, 0] = smax
+    x[:, 1] = v
+    xq, s = oracle_mod.quant_act(x)
+    assert np.all(s == np.float32(smax))
+    assert np.all(xq[:, 0] == 127)
+    exact = 127.0 * v.astype(np.float64) / np.float64(np.float32(smax))
+    assert np.all(np.abs(xq[:, 1] - exact) <= 0.5 + 4e-5)
+    # sign preserved, monotone in v
+    assert np.all(np.sign(xq[:, 1]) * np.sign(v) >= 0)
+    order = np.argsort(v, kind="stable")
+    assert np.all(np.diff(xq[order, 1].astype(np.int32)) >= 0)
+
+
+def test_quant_act_invariants(oracle_mod):
+    rng = np.random.default_rng(5)
+    x = (rng.standard_t(4, size=(64, 777)) * rng.choice([1e-6, 1.0, 1e4])).astype(np.float32)
+    x[3] = 0.0
+    xq, s = oracle_mod.quant_act(x)
+    assert np.all(np.abs(xq.astype(np.int32)) <= 127)  # -128 never produced
+    assert np.all(s[np.arange(64) != 3] == np.abs(x[np.arange(64) != 3]).max(axis=1))
+    assert s[3] == np.float32(1e-8) and np.all(xq[3] == 0)
+    # the element holding the row absmax maps to exactly +/-127
+    idx = np.abs(x).argmax(axis=1)
+    for m in range(64):
+        if m != 3:
+            assert abs(int(xq[m, idx[m]])) == 127
+
+
+# ------------------------------------------------------- contraction ---
+
+def test_contraction_worked_example(oracle_mod):
+    g = load_golden("bitlinear_worked.json")
+    xq = np.array(g["x_q"], dtype=np.int8)
+    acc = oracle_mod.contract(xq, np.array(g["packed"], dtype=np.uint8), g["N"], g["K"])
+    assert acc.tolist() == g["acc"]
+    y = oracle_mod.epilogue(acc, np.array(g["scale"], dtype=np.float32), g["beta"])
+    assert y.tolist() == g["y"]
+
+
+def test_contraction_ternary_product_identity(oracle_mod):
+    # -1*x = -x, 0*x = 0, +1*x = x (BitNet 深度拆解 section 1): with a one-hot
+    # activation v*e_k, acc[n] equals (w[n,k]) * v exactly.
+    rng = np.random.default_rng(9)
+    N, K = 6, 12
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    packed = oracle_mod.pack_codes(q)
+    for k in range(K):
+        for v in (-127, -1, 1, 77, 127):
+            x = np.zeros((1, K), dtype=np.int8)
+            x[0, k] = v
+            acc = oracle_mod.contract(x, packed, N, K)
+            assert acc[0].tolist() == [int(q[n, k]) * v for n in range(N)]
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 4), (3, 5, 8), (4, 7, 20), (2, 9, 100)])
+def test_contraction_equals_fp64_matmul(oracle_mod, M, N, K):
+    # A float64 matmul of the unpacked ternary matrix with x_q is exact for
+    # these magnitudes and must equal the integer accumulator.
+    rng = np.random.default_rng(M * 100 + N * 10 + K)
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    acc = oracle_mod.contract(xq, oracle_mod.pack_codes(q), N, K)
+    ref = xq.astype(np.float64) @ q.astype(np.float64).T
+    assert np.array_equal(acc.astype(np.float64), ref)
+
+
+def test_contraction_equals_sign_mask_loop(oracle_mod):
+    # The sign/mask loop of the devpress post ("三值量化：把乘法变成加减法"):
+    # acc += x if sign > 0 else -x wherever the nonzero mask is set.
+    rng = np.random.default_rng(21)
+    N, K = 5, 16
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    x = rng.integers(-127, 128, size=(1, K)).astype(np.int8)
+    sign = np.where(q >= 0, 1, -1)
+    mask = q != 0
+    out = []
+    for o in range(N):
+        a = 0
+        for i in range(K):
+            if mask[o, i]:
+                a += int(x[0, i]) if sign[o, i] > 0 else -int(x[0, i])
+        out.append(a)
+    acc = oracle_mod.contract(x, oracle_mod.pack_codes(q), N, K)
+    assert acc[0].tolist() == out
+
+
+def test_contraction_row_ranges_and_threads(oracle_mod):
+    rng = np.random.default_rng(2)
+    N, K, M = 37, 64, 3
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    p = oracle_mod.pack_codes(q)
+    full = oracle_mod.contract(xq, p, N, K)
+    assert np.array_equal(oracle_mod.contract(xq, p, N, K, threads=4), full)
+    part = oracle_mod.contract(xq, p, N, K, rows=(10, 20))
+    assert np.array_equal(part[:, 10:20], full[:, 10:20])
+    assert np.all(part[:, :10] == 0) and np.all(part[:, 20:] == 0)
+
+
+# ---------------------------------------------------------- epilogue ---
+
+def test_epilogue_matches_exact_rational(oracle_mod):
+    # y = acc * beta * s / 127 computed exactly with rationals, then rounded to
+    # the nearest fp32: the oracle is within half an fp32 ulp (plus the tiny
+    # fp64 error before the final rounding).
+    rng = np.random.default_rng(4)
+    M, N = 7, 33
+    acc = rng.integers(-2_000_000, 2_000_000, size=(M, N)).astype(np.int32)
+    acc[0, 0] = 0
+    s = (rng.random(M) * 10 + 1e-8).astype(np.float32)
+    beta = np.float32(0.6899)
+    y = oracle_mod.epilogue(acc, s, float(beta))
+    for m in range(M):
+        for n in range(N):
+            exact = Fraction(int(acc[m, n])) * Fraction(float(beta)) * Fraction(float(s[m])) / 127
+            got = Fraction(float(y[m, n]))
+            if exact == 0:
+                assert got == 0
+                continue
+            ulp = Fraction(float(np.spacing(np.float32(abs(float(exact))))))
+            assert abs(got - exact) <= ulp / 2 + abs(exact) * Fraction(1, 10**12)
+
+
+def test_epilogue_zero_beta(oracle_mod):
+    acc = np.array([[5, -7]], dtype=np.int32)
+    assert oracle_mod.epilogue(acc, np.array([3.0], np.float32), 0.0).tolist() == [[0.0, 0.0]]
+
+
+# --------------------------------------------- whole BitLinear forward ---
+
+def test_bitlinear_forward_matches_page_torch_formulation(oracle_mod):
+    # The BitLinear forward of BitNet 深度拆解 section 3.1, run through torch CPU:
+    # F.linear of the integer-valued fp32 operands is exact (|acc| < 2^24), and
+    # the rescale (with weight_scale = beta and act_scale = absmax/127) agrees
+    # with the oracle to fp32 rounding.
+    import torch
+    import torch.nn.functional as F
+
+    rng = np.random.default_rng(12)
+    M, N, K = 4, 96, 256
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    packed, beta, _ = oracle_mod.pack_weights(W)
+    y, acc, xq, s = oracle_mod.bitlinear(x, packed, beta, N, K)
+    wt = torch.from_numpy(oracle_mod.unpack_codes(packed, N * K).reshape(N, K).astype(np.float32))
+    out_q = F.linear(torch.from_numpy(xq.astype(np.float32)), wt)
+    assert np.array_equal(out_q.numpy(), acc.astype(np.float32))
+    ref = (out_q.double() * float(beta) * torch.from_numpy(s).double()[:, None] / 127.0).float()
+    np.testing.assert_allclose(y, ref.numpy(), rtol=1e-6, atol=0)
+    # gamma from torch's own mean agrees with the fixed-order mean here
+    tmean = torch.from_numpy(W).abs().mean()
+    tq = torch.clamp(torch.round((1.0 / (1.0 * tmean + 1e-8)) * torch.from_numpy(W)), -1, 1)
+    assert np.array_equal(tq.numpy().astype(np.int8), wt.numpy().astype(np.int8))
