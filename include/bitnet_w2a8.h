@@ -1,0 +1,161 @@
+/*
+ * bitnet_w2a8.h -- C ABI of the BitNet b1.58 W2A8 ternary-matmul library for
+ * NVIDIA B300 (sm_103a).
+ *
+ * The operations follow these pages (cited by title and section):
+ *   [Deep-dive] "BitNet 深度拆解：当大模型被压到 1.58 bit——从三元权重、BitLinear
+ *               到 bitnet.cpp 的端侧推理革命（2026）"
+ *   [Review]    "BitNet 深度解析：1.58-bit 大模型如何跑向普通 CPU"
+ *
+ * Conventions shared by every call
+ *   - Device pointers are CUDA device (or managed) memory owned by the caller;
+ *     host pointers are named as such.  The library allocates no device
+ *     memory: scratch space is passed in as a caller-owned workspace.
+ *   - Every call validates its arguments on the host before enqueuing
+ *     anything.  On a non-zero status nothing has been enqueued.
+ *   - Calls are asynchronous and stream-ordered on `stream` (0 = legacy
+ *     default stream).  All scalars the kernels consume (beta, scales) live in
+ *     device memory, so calls chain without host synchronisation.
+ *   - Kernels that wait on an on-chip barrier give up after ~1.5 s, set a
+ *     device error word and return; bitnet_check_device_error() reports it.
+ *   - Shapes are int64; every tensor is dense and row-major.
+ *   - The library is thread-compatible: concurrent calls on different
+ *     streams must use different workspaces.
+ */
+#ifndef BITNET_W2A8_H
+#define BITNET_W2A8_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum {
+  BITNET_OK = 0,
+  BITNET_ERR_INVALID_ARG = 1, /* null pointer, unknown dtype, non-finite alpha/eps */
+  BITNET_ERR_SHAPE = 2,       /* M/N/K <= 0, K % 4 != 0, gemv M > 64, size overflow */
+  BITNET_ERR_ALIGNMENT = 3,   /* a float/int32 pointer not aligned to its element size */
+  BITNET_ERR_UNSUPPORTED = 4, /* no sm_103 device / kernel image for this device */
+  BITNET_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+  BITNET_ERR_TIMEOUT = 6,     /* a device-side bounded wait expired */
+  BITNET_ERR_WORKSPACE = 7    /* workspace null or smaller than required */
+} bitnet_status;
+
+/* Element type of floating-point inputs. */
+typedef enum { BITNET_F32 = 0, BITNET_BF16 = 1 } bitnet_dtype;
+
+/* Largest token count bitnet_w2a8_gemv accepts (decode path). */
+#define BITNET_GEMV_MAX_M 64
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *bitnet_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int bitnet_version(void);
+
+/* Workspace bytes bitnet_pack_weights needs for an [N, K] matrix. */
+size_t bitnet_pack_workspace_bytes(int64_t N, int64_t K);
+
+/*
+ * bitnet_pack_weights -- offline absmean ternarisation and 2-bit packing.
+ * [Deep-dive] §2.2 (absmean_quantize), §2.3 (beta), §3.3 (pack_ternary).
+ *
+ *   W        device, [N, K] row-major, dtype BITNET_F32 or BITNET_BF16
+ *            (bf16 is widened exactly to fp32 first).
+ *   alpha,eps host scalars (the pages use 1 and 1e-8).
+ *   packed   device, N*K/4 bytes out.  Element i = n*K + k of the flattened
+ *            matrix is field i%4 (bits 2*(i%4)..+1) of byte i/4, holding code
+ *            w+1 in {0,1,2}.  Row n occupies bytes [n*K/4, (n+1)*K/4).
+ *   beta     device, 1 float out: mean(|W_ternary|) = (#nonzero)/(N*K).
+ *   absmean  device, 1 float out (may be NULL): mean|W| as used for gamma.
+ *   workspace device, >= bitnet_pack_workspace_bytes(N, K) bytes, any contents.
+ *
+ * Arithmetic: S = sum|w| in fp64 over 4096-element chunks of the flattened
+ * matrix, each summed in order, chunk sums added in order; mean = (float)(S/n);
+ * gamma = 1/(fl32(alpha*mean) + eps) in fp32; code = clamp(rint(fl32(gamma*w)),
+ * -1, 1) + 1 with round-half-even (a NaN product gives code 1).
+ * Errors: INVALID_ARG (null W/packed/beta, bad dtype, non-finite alpha or eps),
+ * SHAPE (N, K <= 0, K % 4 != 0), WORKSPACE, CUDA.
+ */
+int bitnet_pack_weights(const void *W, int dtype, int64_t N, int64_t K, float alpha, float eps,
+                        uint8_t *packed, float *beta, float *absmean, void *workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * bitnet_quant_act -- per-token absmax quantisation of activations to int8.
+ * [Deep-dive] §2.2 (absmax_quantize with bits = 8, qmax = 127).
+ *
+ *   x      device, [M, K] row-major, BITNET_F32 or BITNET_BF16.
+ *   x_q    device, [M, K] int8 out: clamp(rint(fl32(fl32(x/s) * 127)), -127, 127).
+ *   scale  device, [M] float out: s = max(max_k |x[m,k]|, fl32(1e-8)) (the
+ *          absmax itself, not absmax/127).
+ * Errors: INVALID_ARG, SHAPE (M, K <= 0), CUDA.
+ */
+int bitnet_quant_act(const void *x, int dtype, int64_t M, int64_t K, int8_t *x_q, float *scale,
+                     cudaStream_t stream);
+
+/* Workspace bytes bitnet_w2a8_gemv needs (0 is never returned). */
+size_t bitnet_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * bitnet_w2a8_gemv -- decode-path ternary matmul with fused dequantisation.
+ * [Deep-dive] §3.1 (integer-domain matmul of W_ternary and X_q), §1 (the
+ * -1/0/+1 products), §2.3 (Y = acc * beta * act_scale); [Review] §03.3 (a W2A8
+ * GEMV is the GPU decode kernel of this method).
+ *
+ *   x_q      device, [M, K] int8 (from bitnet_quant_act), 1 <= M <= 64.
+ *   scale    device, [M] float: per-token absmax s_m.
+ *   packed   device, [N, K/4] bytes in the bitnet_pack_weights format.
+ *   w_scale  device, 1 float: the weight scale (beta, or absmean).
+ *   y        device, [M, N] float out: y = acc * (w_scale * s_m / 127) in fp32.
+ *   acc      device, [M, N] int32 out or NULL: acc = sum_k (code-1) * x_q,
+ *            exact.
+ *   workspace device, >= bitnet_gemv_workspace_bytes(M, N, K) bytes.  Must be
+ *            zero-filled before its first use; every successful call leaves it
+ *            zero-filled again (after BITNET_ERR_TIMEOUT, zero it again).
+ * Packed codes equal to 3 never come out of bitnet_pack_weights; the GEMV
+ * does not define a result for them.
+ * Errors: INVALID_ARG, SHAPE (M outside 1..64, N, K <= 0, K % 4 != 0),
+ * WORKSPACE, CUDA.
+ */
+int bitnet_w2a8_gemv(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
+                     const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc,
+                     void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes bitnet_w2a8_gemm needs. */
+size_t bitnet_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * bitnet_w2a8_gemm -- prefill-path ternary matmul (same operation and
+ * arguments as bitnet_w2a8_gemv, any M >= 1; tuned for M >= 256) on the
+ * tcgen05 tensor cores with TMEM accumulators.  Same citations as the GEMV.
+ *   workspace device, >= bitnet_gemm_workspace_bytes(M, N, K) bytes, any
+ *             contents (the GEMM keeps no state in it between calls).
+ */
+int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
+                     const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc,
+                     void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the
+ * current device.  Returns BITNET_OK, BITNET_ERR_TIMEOUT (a kernel's bounded
+ * wait expired since the last check) or BITNET_ERR_CUDA.
+ */
+int bitnet_check_device_error(cudaStream_t stream);
+
+/*
+ * Enables (1) or disables (0) programmatic dependent launch for the kernels
+ * this thread enqueues: a kernel may then start its weight prefetch while the
+ * previous kernel in the stream is still running.  Off by default.
+ */
+void bitnet_set_pdl(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITNET_W2A8_H */

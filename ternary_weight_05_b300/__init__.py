@@ -1,0 +1,169 @@
+"""BitNet b1.58 W2A8 ternary matmul for NVIDIA B300 (sm_103a).
+
+Thin Python binding over the C ABI of libbitnet_w2a8.so: torch tensors supply
+device memory and the current CUDA stream; every step of the computation runs
+in the library's CUDA kernels.  Function names follow the C entry points.
+
+    packed, beta, absmean = pack_weights(W)          # offline, W [N, K]
+    x_q, scale = quant_act(x)                         # x [M, K] bf16/fp32
+    y = w2a8_gemv(x_q, scale, packed, beta, N, K)     # decode, M <= 64
+    y = w2a8_gemm(x_q, scale, packed, beta, N, K)     # prefill
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import BitnetError
+
+__all__ = [
+    "BitnetError", "pack_weights", "quant_act", "w2a8_gemv", "w2a8_gemm", "bitlinear",
+    "pack_workspace_bytes", "gemv_workspace_bytes", "gemm_workspace_bytes", "check_device_error",
+    "set_pdl", "GEMV_MAX_M", "library_path",
+]
+
+GEMV_MAX_M = 64
+F32, BF16 = 0, 1
+library_path = _lib.LIB_PATH
+
+
+def _L():
+    return _lib.load()
+
+
+def _stream(dev: torch.device) -> int:
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def pack_workspace_bytes(N: int, K: int) -> int:
+    return int(_L().bitnet_pack_workspace_bytes(N, K))
+
+
+def gemv_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_L().bitnet_gemv_workspace_bytes(M, N, K))
+
+
+def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_L().bitnet_gemm_workspace_bytes(M, N, K))
+
+
+def set_pdl(enable: bool) -> None:
+    _L().bitnet_set_pdl(1 if enable else 0)
+
+
+def check_device_error(stream=None) -> None:
+    s = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    _lib.check("bitnet_check_device_error", _L().bitnet_check_device_error(s))
+
+
+class _WorkspaceCache:
+    """Zero-filled device workspaces keyed by (device, kind, shape).
+
+    The GEMV keeps its workspace zero-filled between calls, so one buffer per
+    shape is reused; calls on different streams must not share one.
+    """
+
+    def __init__(self):
+        self._bufs = {}
+
+    def get(self, dev: torch.device, kind: str, nbytes: int, stream_id: int) -> torch.Tensor:
+        key = (dev.index, kind, stream_id)
+        buf = self._bufs.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+            self._bufs[key] = buf
+        return buf
+
+
+_ws = _WorkspaceCache()
+
+
+def pack_weights(W: torch.Tensor, alpha: float = 1.0, eps: float = 1e-8):
+    """Absmean-ternarise and 2-bit pack W [N, K] (fp32 or bf16, on the GPU).
+
+    Returns (packed uint8 [N, K//4], beta float32 [1], absmean float32 [1]).
+    """
+    _dev(W, "W")
+    if W.dim() != 2:
+        raise ValueError("W must be 2-D [N, K]")
+    N, K = W.shape
+    dev = W.device
+    packed = torch.empty((N, K // 4), dtype=torch.uint8, device=dev)
+    beta = torch.empty(1, dtype=torch.float32, device=dev)
+    absmean = torch.empty(1, dtype=torch.float32, device=dev)
+    nbytes = max(pack_workspace_bytes(N, K), 256)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = _L().bitnet_pack_weights(W.data_ptr(), _dtype_code(W), N, K, alpha, eps, packed.data_ptr(),
+                                  beta.data_ptr(), absmean.data_ptr(), ws.data_ptr(), nbytes, _stream(dev))
+    _lib.check("bitnet_pack_weights", st)
+    return packed, beta, absmean
+
+
+def quant_act(x: torch.Tensor, out=None):
+    """Per-token absmax int8 quantisation of x [M, K]: returns (x_q int8, scale f32 [M])."""
+    _dev(x, "x")
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    M, K = x.shape
+    if out is None:
+        x_q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+        scale = torch.empty(M, dtype=torch.float32, device=x.device)
+    else:
+        x_q, scale = out
+    st = _L().bitnet_quant_act(x.data_ptr(), _dtype_code(x), M, K, x_q.data_ptr(), scale.data_ptr(),
+                               _stream(x.device))
+    _lib.check("bitnet_quant_act", st)
+    return x_q, scale
+
+
+def _matmul(fn_name, ws_fn, kind, x_q, scale, packed, w_scale, N, K, want_acc, out, workspace):
+    for t, nm in ((x_q, "x_q"), (scale, "scale"), (packed, "packed"), (w_scale, "w_scale")):
+        _dev(t, nm)
+    M = x_q.shape[0]
+    dev = x_q.device
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=dev)
+    acc = torch.empty((M, N), dtype=torch.int32, device=dev) if want_acc else None
+    nbytes = int(ws_fn(M, N, K))
+    stream = _stream(dev)
+    if workspace is None:
+        workspace = _ws.get(dev, kind, nbytes, stream)
+    st = getattr(_L(), fn_name)(x_q.data_ptr(), scale.data_ptr(), M, packed.data_ptr(), w_scale.data_ptr(), N, K,
+                                y.data_ptr(), acc.data_ptr() if acc is not None else None,
+                                workspace.data_ptr(), workspace.numel(), stream)
+    _lib.check(fn_name, st)
+    return (y, acc) if want_acc else y
+
+
+def w2a8_gemv(x_q, scale, packed, w_scale, N: int, K: int, want_acc: bool = False, out=None, workspace=None):
+    """Decode GEMV (M <= 64): y [M, N] fp32 (and the exact int32 acc if asked)."""
+    return _matmul("bitnet_w2a8_gemv", _L().bitnet_gemv_workspace_bytes, "gemv", x_q, scale, packed, w_scale, N, K,
+                   want_acc, out, workspace)
+
+
+def w2a8_gemm(x_q, scale, packed, w_scale, N: int, K: int, want_acc: bool = False, out=None, workspace=None):
+    """Prefill GEMM (any M): y [M, N] fp32 (and the exact int32 acc if asked)."""
+    return _matmul("bitnet_w2a8_gemm", _L().bitnet_gemm_workspace_bytes, "gemm", x_q, scale, packed, w_scale, N, K,
+                   want_acc, out, workspace)
+
+
+def bitlinear(x: torch.Tensor, packed: torch.Tensor, beta: torch.Tensor, N: int, K: int):
+    """quant_act -> GEMV (M <= 64) or GEMM -> fp32 output [M, N]."""
+    x_q, scale = quant_act(x)
+    if x.shape[0] <= GEMV_MAX_M:
+        return w2a8_gemv(x_q, scale, packed, beta, N, K)
+    return w2a8_gemm(x_q, scale, packed, beta, N, K)

@@ -1,0 +1,340 @@
+// C ABI of the BitNet b1.58 W2A8 library: argument validation, workspace
+// layout, TMA descriptors and kernel launches.  The kernels live in the
+// included .cuh files (one translation unit, so they share the device error
+// word).
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "bitnet_w2a8.h"
+#include "common.cuh"
+#include "gemm.cuh"
+#include "gemv.cuh"
+#include "pack.cuh"
+#include "quant_act.cuh"
+
+using namespace bitnet;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+thread_local int t_pdl = 0;
+
+struct DeviceInfo {
+  bool init = false;
+  int sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  size_t smem_optin = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bitnet_status device_info(DeviceInfo **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BITNET_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo &d = g_dev[dev];
+  if (!d.init) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return BITNET_ERR_CUDA;
+    d.sms = prop.multiProcessorCount;
+    d.cc_major = prop.major;
+    d.cc_minor = prop.minor;
+    d.smem_optin = prop.sharedMemPerBlockOptin;
+    d.init = true;
+  }
+  if (d.cc_major != 10 || d.cc_minor != 3) return BITNET_ERR_UNSUPPORTED;
+  *out = &d;
+  return BITNET_OK;
+}
+
+bitnet_status get_encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return BITNET_OK;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return BITNET_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return BITNET_OK;
+}
+
+// Launches `kernel` with optional programmatic dependent launch.
+template <typename... KArgs, typename... Args>
+bitnet_status launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (t_pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return e == cudaSuccess ? BITNET_OK : BITNET_ERR_CUDA;
+}
+
+template <typename K>
+bitnet_status set_smem(K kernel, size_t bytes) {
+  // cudaFuncSetAttribute is cheap and per device; it is called on every
+  // launch that needs more than the default 48 KB.
+  if (bytes <= 48 * 1024) return BITNET_OK;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess
+             ? BITNET_OK
+             : BITNET_ERR_CUDA;
+}
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+constexpr int64_t kMaxElems = (int64_t)1 << 40;
+
+bool shape_ok(int64_t N, int64_t K) { return N > 0 && K > 0 && K % 4 == 0 && N <= kMaxElems / K; }
+
+// ------------------------------------------------------------------ GEMV --
+
+struct GemvPlan {
+  bool tma;
+  int NR, NKB, KBS, S, xrow, grid;
+  bool hmma;
+  size_t smem;
+  size_t ws_partial_bytes, ws_bytes;
+};
+
+GemvPlan plan_gemv(int64_t M, int64_t N, int64_t K, int sms) {
+  GemvPlan pl = {};
+  pl.NR = (int)cdiv(N, kStageRows);
+  pl.NKB = (int)cdiv(K, kStageK);
+  pl.hmma = M > 2;
+  const int per_kb = pl.hmma ? 1024 : 512;  // activation bytes per token per K-block
+  int kbs_max = (int)((kGemvXBudget / M - (pl.hmma ? 8 : 0)) / per_kb);
+  kbs_max = std::max(1, kbs_max);
+  pl.S = (int)cdiv(pl.NKB, kbs_max);
+  pl.KBS = (int)cdiv(pl.NKB, pl.S);
+  pl.xrow = pl.hmma ? pl.KBS * 1024 + 8 : pl.KBS * 512;
+  const long long total = (long long)pl.NR * pl.NKB;
+  pl.grid = (int)std::min<long long>(sms, total);
+  pl.smem = gemv_smem_layout((int)M, pl.KBS, pl.xrow).bytes + 1024;
+  pl.ws_partial_bytes = (size_t)pl.NR * kStageRows * M * 4;
+  pl.ws_bytes = pl.ws_partial_bytes + (size_t)pl.NR * 4 + 256;
+  return pl;
+}
+
+template <class Policy>
+bitnet_status launch_gemv_tma(const CUtensorMap &map, const GemvParams &p, const GemvPlan &pl,
+                              cudaStream_t stream) {
+  auto k = gemv_tma_kernel<Policy>;
+  if (set_smem(k, pl.smem) != BITNET_OK) return BITNET_ERR_CUDA;
+  return launch(k, dim3(pl.grid), dim3(kGemvThreads), pl.smem, stream, map, p);
+}
+
+bitnet_status encode_packed_map(CUtensorMap *map, const uint8_t *packed, int64_t N, int64_t K, uint32_t box_x,
+                                uint32_t box_y, CUtensorMapSwizzle swz) {
+  if (get_encoder() != BITNET_OK) return BITNET_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)(K / 4), (cuuint64_t)N};
+  cuuint64_t strides[1] = {(cuuint64_t)(K / 4)};
+  cuuint32_t box[2] = {box_x, box_y};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(packed), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BITNET_OK : BITNET_ERR_CUDA;
+}
+
+bitnet_status check_gemm_args(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
+                              const float *w_scale, int64_t N, int64_t K, float *y, void *ws) {
+  if (!x_q || !scale || !packed || !w_scale || !y) return BITNET_ERR_INVALID_ARG;
+  if (M <= 0 || !shape_ok(N, K) || M > kMaxElems / K || M > kMaxElems / N) return BITNET_ERR_SHAPE;
+  if (!aligned(scale, 4) || !aligned(w_scale, 4) || !aligned(y, 4)) return BITNET_ERR_ALIGNMENT;
+  if (!ws) return BITNET_ERR_WORKSPACE;
+  return BITNET_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *bitnet_status_string(int status) {
+  switch (status) {
+    case BITNET_OK: return "BITNET_OK";
+    case BITNET_ERR_INVALID_ARG: return "BITNET_ERR_INVALID_ARG";
+    case BITNET_ERR_SHAPE: return "BITNET_ERR_SHAPE";
+    case BITNET_ERR_ALIGNMENT: return "BITNET_ERR_ALIGNMENT";
+    case BITNET_ERR_UNSUPPORTED: return "BITNET_ERR_UNSUPPORTED";
+    case BITNET_ERR_CUDA: return "BITNET_ERR_CUDA";
+    case BITNET_ERR_TIMEOUT: return "BITNET_ERR_TIMEOUT";
+    case BITNET_ERR_WORKSPACE: return "BITNET_ERR_WORKSPACE";
+    default: return "BITNET_ERR_UNKNOWN";
+  }
+}
+
+int bitnet_version(void) { return 100; }
+
+void bitnet_set_pdl(int enable) { t_pdl = enable ? 1 : 0; }
+
+size_t bitnet_pack_workspace_bytes(int64_t N, int64_t K) {
+  if (!shape_ok(N, K)) return 0;
+  return kPackScratchHeader + (size_t)cdiv(N * K, kAbsChunk) * sizeof(double);
+}
+
+int bitnet_pack_weights(const void *W, int dtype, int64_t N, int64_t K, float alpha, float eps, uint8_t *packed,
+                        float *beta, float *absmean, void *workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+  if (!W || !packed || !beta) return BITNET_ERR_INVALID_ARG;
+  if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha) || !std::isfinite(eps)) return BITNET_ERR_INVALID_ARG;
+  if (!shape_ok(N, K)) return BITNET_ERR_SHAPE;
+  if (!aligned(W, dtype == BITNET_F32 ? 4 : 2) || !aligned(beta, 4) || !aligned(absmean, 4))
+    return BITNET_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < bitnet_pack_workspace_bytes(N, K) || !aligned(workspace, 8))
+    return BITNET_ERR_WORKSPACE;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
+  const int64_t n = N * K;
+  const int64_t nchunks = cdiv(n, kAbsChunk);
+  PackScratch *scr = reinterpret_cast<PackScratch *>(workspace);
+  double *sums = reinterpret_cast<double *>(reinterpret_cast<uint8_t *>(workspace) + kPackScratchHeader);
+  const dim3 cgrid((unsigned)cdiv(nchunks, kPackThreads));
+  const int64_t nwords = n / 16;
+  const dim3 pgrid((unsigned)std::max<int64_t>(1, std::min<int64_t>(cdiv(nwords, kPackThreads), d->sms * 16)));
+  const bool word_store = aligned(packed, 4);
+  bitnet_status st;
+  if (dtype == BITNET_F32) {
+    const float *w = static_cast<const float *>(W);
+    st = launch(pack_chunk_sums_kernel<float>, cgrid, dim3(kPackThreads), 0, stream, w, n, sums);
+    if (!st) st = launch(pack_finalize_kernel, dim3(1), dim3(32), 0, stream, (const double *)sums, nchunks, n,
+                         alpha, eps, scr, absmean);
+    if (!st)
+      st = word_store ? launch(pack_codes_kernel<float, true>, pgrid, dim3(kPackThreads), 0, stream, w, n, packed, scr)
+                      : launch(pack_codes_kernel<float, false>, pgrid, dim3(kPackThreads), 0, stream, w, n, packed,
+                               scr);
+  } else {
+    const __nv_bfloat16 *w = static_cast<const __nv_bfloat16 *>(W);
+    st = launch(pack_chunk_sums_kernel<__nv_bfloat16>, cgrid, dim3(kPackThreads), 0, stream, w, n, sums);
+    if (!st) st = launch(pack_finalize_kernel, dim3(1), dim3(32), 0, stream, (const double *)sums, nchunks, n,
+                         alpha, eps, scr, absmean);
+    if (!st)
+      st = word_store ? launch(pack_codes_kernel<__nv_bfloat16, true>, pgrid, dim3(kPackThreads), 0, stream, w, n,
+                               packed, scr)
+                      : launch(pack_codes_kernel<__nv_bfloat16, false>, pgrid, dim3(kPackThreads), 0, stream, w, n,
+                               packed, scr);
+  }
+  if (!st) st = launch(pack_beta_kernel, dim3(1), dim3(32), 0, stream, (const PackScratch *)scr, n, beta);
+  return st;
+}
+
+int bitnet_quant_act(const void *x, int dtype, int64_t M, int64_t K, int8_t *x_q, float *scale,
+                     cudaStream_t stream) {
+  if (!x || !x_q || !scale) return BITNET_ERR_INVALID_ARG;
+  if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_ERR_INVALID_ARG;
+  if (M <= 0 || K <= 0 || M > kMaxElems / K || M > 0x7fffffff) return BITNET_ERR_SHAPE;
+  if (!aligned(x, dtype == BITNET_F32 ? 4 : 2) || !aligned(scale, 4)) return BITNET_ERR_ALIGNMENT;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
+  const size_t esz = dtype == BITNET_F32 ? 4 : 2;
+  const bool vec = aligned(x, 16) && ((K * (int64_t)esz) % 16 == 0) && (K % 8 == 0) && aligned(x_q, 8);
+  const dim3 grid((unsigned)M), block(kQuantThreads);
+  if (dtype == BITNET_F32) {
+    const float *xp = static_cast<const float *>(x);
+    return vec ? launch(quant_act_kernel<float, true>, grid, block, 0, stream, xp, K, x_q, scale)
+               : launch(quant_act_kernel<float, false>, grid, block, 0, stream, xp, K, x_q, scale);
+  }
+  const __nv_bfloat16 *xp = static_cast<const __nv_bfloat16 *>(x);
+  return vec ? launch(quant_act_kernel<__nv_bfloat16, true>, grid, block, 0, stream, xp, K, x_q, scale)
+             : launch(quant_act_kernel<__nv_bfloat16, false>, grid, block, 0, stream, xp, K, x_q, scale);
+}
+
+size_t bitnet_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || M > BITNET_GEMV_MAX_M || !shape_ok(N, K)) return 0;
+  return plan_gemv(M, N, K, 148).ws_bytes;
+}
+
+int bitnet_w2a8_gemv(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
+                     const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc, void *workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
+  if (bitnet_status s = check_gemm_args(x_q, scale, M, packed, w_scale, N, K, y, workspace)) return s;
+  if (!aligned(acc, 4)) return BITNET_ERR_ALIGNMENT;
+  if (M > BITNET_GEMV_MAX_M) return BITNET_ERR_SHAPE;
+  if (N > 0x7fffffff || K > 0x7fffffff) return BITNET_ERR_SHAPE;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
+  GemvPlan pl = plan_gemv(M, N, K, d->sms);
+  if (workspace_bytes < pl.ws_bytes || !aligned(workspace, 16)) return BITNET_ERR_WORKSPACE;
+
+  GemvParams p = {};
+  p.packed = packed;
+  p.xq = x_q;
+  p.scale = scale;
+  p.w_scale = w_scale;
+  p.y = y;
+  p.acc = acc;
+  p.ws_partial = static_cast<int32_t *>(workspace);
+  p.ws_ticket = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(workspace) + pl.ws_partial_bytes);
+  p.N = N;
+  p.K = K;
+  p.M = (int)M;
+  p.NR = pl.NR;
+  p.NKB = pl.NKB;
+  p.KBS = pl.KBS;
+  p.S = pl.S;
+  p.xrow = pl.xrow;
+  p.total = (long long)pl.NR * pl.NKB;
+
+  const bool tma_ok = (K % 64 == 0) && K >= kStageK && aligned(packed, 16);
+  if (!tma_ok) {
+    const long long items = (long long)N * M;
+    const int blocks = (int)std::min<long long>(cdiv(items, 8), (long long)d->sms * 16);
+    return launch(gemv_generic_kernel, dim3(blocks), dim3(256), 0, stream, p);
+  }
+  CUtensorMap map;
+  if (bitnet_status s = encode_packed_map(&map, packed, N, K, kStageRowBytes, kStageRows,
+                                          CU_TENSOR_MAP_SWIZZLE_128B))
+    return s;
+  switch (M) {
+    case 1: return launch_gemv_tma<Dp4aPolicy<1>>(map, p, pl, stream);
+    case 2: return launch_gemv_tma<Dp4aPolicy<2>>(map, p, pl, stream);
+    default: break;
+  }
+  if (M <= 8) return launch_gemv_tma<HmmaPolicy<1, 4, 1>>(map, p, pl, stream);
+  if (M <= 16) return launch_gemv_tma<HmmaPolicy<2, 4, 1>>(map, p, pl, stream);
+  if (M <= 32) return launch_gemv_tma<HmmaPolicy<4, 2, 2>>(map, p, pl, stream);
+  return launch_gemv_tma<HmmaPolicy<8, 1, 4>>(map, p, pl, stream);
+}
+
+size_t bitnet_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || !shape_ok(N, K)) return 0;
+  return gemm_workspace_bytes(M, N, K);
+}
+
+int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
+                     const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc, void *workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
+  if (bitnet_status s = check_gemm_args(x_q, scale, M, packed, w_scale, N, K, y, workspace)) return s;
+  if (workspace_bytes < gemm_workspace_bytes(M, N, K)) return BITNET_ERR_WORKSPACE;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
+  return gemm_launch(x_q, scale, M, packed, w_scale, N, K, y, acc, workspace, d->sms, stream);
+}
+
+int bitnet_check_device_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return BITNET_ERR_CUDA;
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return BITNET_ERR_CUDA;
+  if (v == 0) return BITNET_OK;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) return BITNET_ERR_CUDA;
+  return BITNET_ERR_TIMEOUT;
+}
+
+}  // extern "C"

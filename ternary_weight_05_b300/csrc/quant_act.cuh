@@ -1,0 +1,98 @@
+// Per-token absmax activation quantisation to int8.
+//
+// BitNet 深度拆解 §2.2 (absmax_quantize, bits = 8): the scale of token m is
+// s = max(max_k |x[m,k]|, 1e-8) and q = clamp(round(x / s * 127), -127, 127),
+// with round-half-even.  Every operation is the single IEEE fp32 operation
+// the formula names (division first, then the multiply by 127).
+//
+// One CTA per token row; two passes over the row (the second hits L1/L2).
+#pragma once
+
+#include "common.cuh"
+
+namespace bitnet {
+
+constexpr int kQuantThreads = 256;
+
+__device__ __forceinline__ int8_t quantize_one(float v, float s) {
+  const float r = __fmul_rn(__fdiv_rn(v, s), 127.0f);
+  int q = __float2int_rn(r);
+  q = q > 127 ? 127 : (q < -127 ? -127 : q);
+  return static_cast<int8_t>(q);
+}
+
+__device__ __forceinline__ float block_max_256(float v, float *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < kQuantThreads / 32; ++w) r = fmaxf(r, red[w]);
+  return r;
+}
+
+// 8 consecutive elements as fp32 (exact widening for bf16).
+__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4 *>(p)[0];
+  const float4 b = reinterpret_cast<const float4 *>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4 *>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// VEC: the row start of x is 16-byte aligned, K is a multiple of 8 and the
+// x_q row start is 8-byte aligned, so 8 elements move per access.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const T *__restrict__ x, int64_t K,
+                                                                  int8_t *__restrict__ xq,
+                                                                  float *__restrict__ scale) {
+  __shared__ float red[kQuantThreads / 32];
+  pdl_wait_prior_grid();
+  pdl_launch_dependents();
+  const int64_t m = blockIdx.x;
+  const T *row = x + m * K;
+  int8_t *qrow = xq + m * K;
+
+  float amax = 0.0f;
+  if (VEC) {
+    for (int64_t k = (int64_t)threadIdx.x * 8; k < K; k += kQuantThreads * 8) {
+      float v[8];
+      load8(row + k, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    }
+  } else {
+    for (int64_t k = threadIdx.x; k < K; k += kQuantThreads) amax = fmaxf(amax, fabsf(load_as_f32(row, k)));
+  }
+  amax = block_max_256(amax, red);
+  const float s = amax < 1e-8f ? 1e-8f : amax;
+  if (threadIdx.x == 0) scale[m] = s;
+
+  if (VEC) {
+    for (int64_t k = (int64_t)threadIdx.x * 8; k < K; k += kQuantThreads * 8) {
+      float v[8];
+      load8(row + k, v);
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) lo |= (uint32_t)(uint8_t)quantize_one(v[i], s) << (8 * i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hi |= (uint32_t)(uint8_t)quantize_one(v[4 + i], s) << (8 * i);
+      *reinterpret_cast<uint2 *>(qrow + k) = make_uint2(lo, hi);
+    }
+  } else {
+    for (int64_t k = threadIdx.x; k < K; k += kQuantThreads) qrow[k] = quantize_one(load_as_f32(row, k), s);
+  }
+}
+
+}  // namespace bitnet

@@ -1,0 +1,118 @@
+"""The C-ABI library loads, exports every declared symbol and rejects bad
+arguments on the host before touching the GPU (no GPU needed)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+INVALID_ARG, SHAPE, WORKSPACE = 1, 2, 7
+
+
+@pytest.fixture(scope="module")
+def clib():
+    from ternary_weight_05_b300 import _lib, build
+
+    build.build()
+    return _lib.load()
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b(bitnet_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ["bitnet_pack_weights", "bitnet_quant_act", "bitnet_w2a8_gemv", "bitnet_w2a8_gemm"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(clib):
+    from ternary_weight_05_b300 import _lib
+
+    for name in declared_symbols():
+        assert hasattr(clib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(clib):
+    assert clib.bitnet_status_string(0) == b"BITNET_OK"
+    assert clib.bitnet_status_string(6) == b"BITNET_ERR_TIMEOUT"
+    assert clib.bitnet_status_string(99) == b"BITNET_ERR_UNKNOWN"
+    assert clib.bitnet_version() >= 100
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def test_quant_act_validation(clib):
+    assert clib.bitnet_quant_act(None, 0, 1, 8, FAKE, FAKE, None) == INVALID_ARG
+    assert clib.bitnet_quant_act(FAKE, 3, 1, 8, FAKE, FAKE, None) == INVALID_ARG
+    assert clib.bitnet_quant_act(FAKE, 0, 0, 8, FAKE, FAKE, None) == SHAPE
+    assert clib.bitnet_quant_act(FAKE, 1, 4, -1, FAKE, FAKE, None) == SHAPE
+
+
+def test_pack_validation(clib):
+    ws = clib.bitnet_pack_workspace_bytes(16, 64)
+    assert ws >= 256 + 8
+    assert clib.bitnet_pack_workspace_bytes(16, 6) == 0
+    args = lambda **kw: dict(dict(W=FAKE, dt=0, N=16, K=64, a=1.0, e=1e-8, p=FAKE, b=FAKE, am=None, ws=FAKE,
+                                  wsb=ws), **kw)
+
+    def call(**kw):
+        a = args(**kw)
+        return clib.bitnet_pack_weights(a["W"], a["dt"], a["N"], a["K"], a["a"], a["e"], a["p"], a["b"], a["am"],
+                                        a["ws"], a["wsb"], None)
+
+    assert call(W=None) == INVALID_ARG
+    assert call(p=None) == INVALID_ARG
+    assert call(dt=5) == INVALID_ARG
+    assert call(a=float("nan")) == INVALID_ARG
+    assert call(e=float("inf")) == INVALID_ARG
+    assert call(K=6) == SHAPE
+    assert call(N=0) == SHAPE
+    assert call(ws=None) == WORKSPACE
+    assert call(wsb=ws - 1) == WORKSPACE
+
+
+@pytest.mark.parametrize("fn", ["bitnet_w2a8_gemv", "bitnet_w2a8_gemm"])
+def test_matmul_validation(clib, fn):
+    f = getattr(clib, fn)
+
+    def call(xq=FAKE, s=FAKE, M=1, p=FAKE, ws_=FAKE, N=8, K=64, y=FAKE, work=FAKE, wb=1 << 20):
+        return f(xq, s, M, p, ws_, N, K, y, None, work, wb, None)
+
+    assert call(xq=None) == INVALID_ARG
+    assert call(y=None) == INVALID_ARG
+    assert call(ws_=None) == INVALID_ARG
+    assert call(K=10) == SHAPE
+    assert call(M=0) == SHAPE
+    assert call(N=-3) == SHAPE
+    assert call(work=None) == WORKSPACE
+    if fn == "bitnet_w2a8_gemv":
+        assert call(M=65) == SHAPE
+
+
+def test_workspace_sizes_cover_partials(clib):
+    for M, N, K in [(1, 2560, 2560), (16, 28672, 8192), (64, 13824, 2560), (3, 129, 1000)]:
+        nb = clib.bitnet_gemv_workspace_bytes(M, N, K)
+        assert nb >= ((N + 127) // 128) * 128 * M * 4
+    assert clib.bitnet_gemv_workspace_bytes(65, 8, 64) == 0
+    assert clib.bitnet_gemm_workspace_bytes(2048, 6912, 2560) > 0
+
+
+def test_package_fails_loudly_without_library(tmp_path, monkeypatch):
+    from ternary_weight_05_b300 import _lib
+
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(ImportError):
+        _lib.load()
