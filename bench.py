@@ -1,0 +1,509 @@
+#!/usr/bin/env python3
+"""Throughput of the BitNet b1.58 W2A8 path on B300: packed-weight GB/s.
+
+One step = one decode pass of one token through a stack of BitLinear layers
+shaped like a ~2B BitNet model (per layer: q/o 2560x2560, gate/up 6912x2560,
+down 2560x6912; 30 layers, 496 MB of packed 2-bit weights, about 4x the L2),
+each GEMV preceded by the per-token int8 quantisation of its own activation.
+Weights are packed once before timing (offline step).  The stack is larger
+than L2, so every step reads its weights from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own copy
+of the stack (independent token streams, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W2A8 GEMV packed-weight GB/s (% of HBM peak); prefill GEMM int8 TOPS (% peak)"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="2b-decode",
+                    choices=["2b-decode", "100b-stream", "gateup-sweep", "prefill-2048", "bitlinear-1024"])
+    ap.add_argument("--layers", type=int, default=30)
+    ap.add_argument("--M", type=int, default=None, help="tokens (decode workloads)")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1400.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during timing."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ workloads --
+
+def decode_layers(args):
+    from ternary_weight_05_b300 import synth
+
+    if args.workload == "2b-decode":
+        wl = synth.workload("2b-decode")
+        layers = [(L, rep) for rep in range(args.layers) for L in wl.layers]
+        M = args.M or 1
+    elif args.workload == "100b-stream":
+        wl = synth.workload("100b-stream")
+        layers = [(L, 0) for L in wl.layers[: args.layers]]
+        M = args.M or 1
+    elif args.workload == "gateup-sweep":
+        wl = synth.workload("gateup-sweep")
+        layers = [(wl.layers[0], r) for r in range(max(1, args.layers))]
+        M = args.M or 1
+    elif args.workload == "bitlinear-1024":
+        wl = synth.workload("bitlinear-1024")
+        layers = [(wl.layers[0], r) for r in range(max(1, args.layers))]
+        M = 1
+    else:
+        raise ValueError(args.workload)
+    return wl, layers, M
+
+
+def build_stack(args, dev, rank):
+    """Packs every weight matrix on the device (offline step, not timed)."""
+    import torch
+
+    import ternary_weight_05_b300 as tw
+    from ternary_weight_05_b300 import synth
+
+    wl, layers, M = decode_layers(args)
+    stack = []
+    for L, rep in layers:
+        W = synth.weights_torch(L.N, L.K, L.w_dist, L.w_scale, L.w_seed + 1000 * rep, dev)
+        packed, beta, _ = tw.pack_weights(W)
+        del W
+        x = synth.acts_torch(M, L.K, L.x_dist, L.x_seed + 1000 * rep + 7919 * rank, dev, outlier_p=L.outlier_p)
+        if not L.x_bf16:
+            x = x.float()
+        stack.append(dict(L=L, packed=packed, beta=beta, x=x, M=M,
+                          xq=torch.empty((M, L.K), dtype=torch.int8, device=dev),
+                          s=torch.empty(M, dtype=torch.float32, device=dev),
+                          y=torch.empty((M, L.N), dtype=torch.float32, device=dev)))
+    torch.cuda.synchronize(dev)
+    return wl, stack, M
+
+
+def init_dist():
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    return world, rank, dev
+
+
+def run_native(args):
+    import torch
+    import torch.distributed as dist
+
+    import ternary_weight_05_b300 as tw
+
+    world, rank, dev = init_dist()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
+    if args.workload == "prefill-2048":
+        return run_prefill(args, dev, rank, world, bf16_peak, peak_src)
+
+    wl, stack, M = build_stack(args, dev, rank)
+    max_ws = max(tw.gemv_workspace_bytes(M, e["L"].N, e["L"].K) for e in stack)
+    ws = torch.zeros(max_ws, dtype=torch.uint8, device=dev)
+    wbytes = sum(e["L"].N * e["L"].K // 4 for e in stack)
+    # algorithmic bytes of the GEMV: packed weights + x_q + scales + y
+    gemv_bytes = sum(e["L"].N * e["L"].K // 4 + M * e["L"].K + 4 * M + 4 * M * e["L"].N + 4 for e in stack)
+
+    def step():
+        for e in stack:
+            tw.quant_act(e["x"], out=(e["xq"], e["s"]))
+            tw.w2a8_gemv(e["xq"], e["s"], e["packed"], e["beta"], e["L"].N, e["L"].K, out=e["y"], workspace=ws)
+
+    tw.set_pdl(not args.no_pdl)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        step()
+        torch.cuda.synchronize(dev)
+        graph = None
+        if not args.no_graph:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                step()
+        run = graph.replay if graph is not None else step
+        for _ in range(args.warmup):
+            run()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        clocks = ClockSampler(dev.index or 0)
+        clocks.start()
+        time.sleep(0.3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_total = e0.elapsed_time(e1)
+
+        # GEMV kernel duration: a graph holding only the GEMV launches of the
+        # stack (same inputs, same launch configuration, weights colder than
+        # L2 since the stack exceeds it), replayed between two events.
+        gemv_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gemv_graph, stream=stream):
+            for e in stack:
+                tw.w2a8_gemv(e["xq"], e["s"], e["packed"], e["beta"], e["L"].N, e["L"].K, out=e["y"],
+                             workspace=ws)
+        for _ in range(2):
+            gemv_graph.replay()
+        n_meas = max(3, args.steps)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(n_meas):
+            gemv_graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop()
+        gemv_ms = g0.elapsed_time(g1)
+        gemv_launches = n_meas * len(stack)
+
+        # end to end through the public API with host buffers
+        tw.set_pdl(False)
+        hx = [e["x"].cpu().pin_memory() for e in stack]
+        hy = [torch.empty(e["y"].shape, dtype=torch.float32).pin_memory() for e in stack]
+        h2d = sum(t.numel() * t.element_size() for t in hx)
+        d2h = sum(t.numel() * t.element_size() for t in hy)
+
+        def e2e_step():
+            for e, xh, yh in zip(stack, hx, hy):
+                xd = xh.to(dev, non_blocking=True)
+                y = tw.bitlinear(xd, e["packed"], e["beta"], e["L"].N, e["L"].K)
+                yh.copy_(y, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e2e_s = time.perf_counter() - t0
+    tw.check_device_error(stream)
+
+    ms_step = ms_total / args.steps
+    if world > 1:  # max over ranks
+        t = torch.tensor([ms_step, e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, e2e_s = t[0].item(), t[1].item()
+    value = world * wbytes / (ms_step * 1e-3) / 1e9
+    e2e_val = world * wbytes * args.steps / e2e_s / 1e9
+    achieved = gemv_bytes * n_meas / (gemv_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded, weights and activations drawn on device)",
+        "config": {"workload": f"{wl.name}: {wl.description}", "layers_in_stack": len(stack), "M": M,
+                   "packed_weight_bytes_per_step": wbytes, "graph": not args.no_graph, "pdl": not args.no_pdl,
+                   "l2": "inputs larger than L2 (packed stack %.0f MB > 126 MB L2)" % (wbytes / 1e6),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "kernel": "gemv_rows_kernel" if M <= 2 else "gemv_tma_kernel", "peak_source": peak_src,
+                     "launches_timed": gemv_launches, "avg_launch_us": round(1e3 * gemv_ms / gemv_launches, 3)},
+        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * len(stack) * args.steps,
+        "gemv_only_GBps": round(wbytes * n_meas / (gemv_ms * 1e-3) / 1e9, 2),
+        "clocks": clk,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
+    """Prefill: per step, quant_act + tcgen05 GEMM for both M=2048 matrices.
+    L2 is flushed (256 MB write) between steps, outside the timed spans."""
+    import torch
+    import torch.distributed as dist
+
+    import ternary_weight_05_b300 as tw
+    from ternary_weight_05_b300 import synth
+
+    wl = synth.workload("prefill-2048")
+    M = args.M or 2048
+    mats = []
+    for L in wl.layers:
+        W = synth.weights_torch(L.N, L.K, L.w_dist, L.w_scale, L.w_seed, dev)
+        packed, beta, _ = tw.pack_weights(W)
+        x = synth.acts_torch(M, L.K, L.x_dist, L.x_seed + 7919 * rank, dev)
+        mats.append(dict(L=L, packed=packed, beta=beta, x=x,
+                         xq=torch.empty((M, L.K), dtype=torch.int8, device=dev),
+                         s=torch.empty(M, dtype=torch.float32, device=dev),
+                         y=torch.empty((M, L.N), dtype=torch.float32, device=dev),
+                         ws=torch.empty(tw.gemm_workspace_bytes(M, L.N, L.K), dtype=torch.uint8, device=dev)))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flops = sum(2.0 * M * m["L"].N * m["L"].K for m in mats)
+    tw.set_pdl(not args.no_pdl)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        def step():
+            for m in mats:
+                tw.quant_act(m["x"], out=(m["xq"], m["s"]))
+                tw.w2a8_gemm(m["xq"], m["s"], m["packed"], m["beta"], m["L"].N, m["L"].K, out=m["y"],
+                             workspace=m["ws"])
+
+        def gemm_only():
+            for m in mats:
+                tw.w2a8_gemm(m["xq"], m["s"], m["packed"], m["beta"], m["L"].N, m["L"].K, out=m["y"],
+                             workspace=m["ws"])
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        clocks = ClockSampler(dev.index or 0)
+        clocks.start()
+        time.sleep(0.3)
+        spans, gspans = [], []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step()
+            b.record(stream)
+            spans.append((a, b))
+        for _ in range(args.steps):
+            flush.fill_(2)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            gemm_only()
+            b.record(stream)
+            gspans.append((a, b))
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop()
+        ms_step = sum(a.elapsed_time(b) for a, b in spans) / args.steps
+        ms_gemm = sum(a.elapsed_time(b) for a, b in gspans) / args.steps
+        # end to end: host activations in, host outputs out, public API
+        tw.set_pdl(False)
+        hx = [m["x"].cpu().pin_memory() for m in mats]
+        hy = [torch.empty(m["y"].shape, dtype=torch.float32).pin_memory() for m in mats]
+
+        def e2e_step():
+            for m, xh, yh in zip(mats, hx, hy):
+                y = tw.bitlinear(xh.to(dev, non_blocking=True), m["packed"], m["beta"], m["L"].N, m["L"].K)
+                yh.copy_(y, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e2e_s = (time.perf_counter() - t0) / args.steps
+    tw.check_device_error(stream)
+    if world > 1:
+        t = torch.tensor([ms_step, e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, e2e_s = t[0].item(), t[1].item()
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    achieved = flops / (ms_gemm * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded, drawn on device)",
+        "config": {"workload": f"{wl.name}: {wl.description}", "M": M,
+                   "matrices": [f"{m['L'].N}x{m['L'].K}" for m in mats], "l2": "flushed between steps (256 MB)",
+                   "pdl": not args.no_pdl, "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / bf16_peak, 4), "traffic": None, "kernel": "gemm_tc_kernel (+prep)",
+                     "peak_source": peak_src + " bf16 dense burst (the GEMM runs kind::f16 MMAs)"},
+        "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TOPS",
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hx),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hy)},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = {"value": None, "unit": "TOPS", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": "not run for the prefill workload"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def oracle_sample(args):
+    """Host copies of one layer of the workload for the oracle (bounded sample)."""
+    import oracle
+    from ternary_weight_05_b300 import synth
+
+    wl, layers, M = decode_layers(args)
+    n = len(wl.layers) if args.workload == "2b-decode" else 1
+    sample = []
+    for L, rep in layers[:n]:
+        W = synth.weights_np(L.N, L.K, L.w_dist, L.w_scale, seed=L.w_seed + 1000 * rep)
+        packed, beta, _ = oracle.pack_weights(W)
+        _, x = synth.acts_np(M, L.K, L.x_dist, seed=L.x_seed + 1000 * rep, outlier_p=L.outlier_p, bf16=L.x_bf16)
+        sample.append((L, packed, beta, x))
+    return sample, M
+
+
+def time_oracle(sample, seconds, threads):
+    import oracle
+
+    done_bytes, t0, passes = 0, time.perf_counter(), 0
+    while True:
+        for L, packed, beta, x in sample:
+            oracle.bitlinear(x, packed, beta, L.N, L.K, threads=threads)
+            done_bytes += L.N * L.K // 4
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return done_bytes / el / 1e9, el, passes
+
+
+def cpu_baseline(args):
+    try:
+        sample, M = oracle_sample(args)
+        cores = os.cpu_count() or 1
+        gbs, el, passes = time_oracle(sample, args.cpu_seconds, cores)
+        names = ",".join(L.name for L, *_ in sample)
+        return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                "sample": f"{passes} pass(es) over one layer ({names}; M={M}) in {el:.1f} s, "
+                          f"rows split over {cores} threads"}
+    except Exception as ex:  # the baseline must never break the GPU line
+        return {"value": None, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle", "sample": f"failed: {ex}"}
+
+
+def run_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    sample, M = oracle_sample(args)
+    cores = os.cpu_count() or 1
+    per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        time_oracle(sample, per_step / 4, cores)
+    vals = []
+    for _ in range(args.steps):
+        gbs, _, _ = time_oracle(sample, per_step, cores)
+        vals.append(gbs)
+    value = statistics.median(vals)
+    wbytes = sum(L.N * L.K // 4 for L, *_ in sample)
+    names = ",".join(L.name for L, *_ in sample)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * wbytes / (value * 1e9), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic (seeded numpy PCG64)",
+        "config": {"workload": args.workload, "M": M, "sample": f"one layer ({names}) per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: >= {per_step:.1f} s of passes over one layer ({names}), "
+                                   f"rows split over {cores} threads"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

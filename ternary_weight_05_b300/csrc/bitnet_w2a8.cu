@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "gemm.cuh"
 #include "gemv.cuh"
+#include "gemv_rows.cuh"
 #include "pack.cuh"
 #include "quant_act.cuh"
 
@@ -298,6 +299,30 @@ int bitnet_w2a8_gemv(const int8_t *x_q, const float *scale, int64_t M, const uin
     const int blocks = (int)std::min<long long>(cdiv(items, 8), (long long)d->sms * 16);
     return launch(gemv_generic_kernel, dim3(blocks), dim3(256), 0, stream, p);
   }
+  if (M <= 2 && M * cdiv(K, kStageK) * kStageK <= kRowsXBudget) {
+    // one or two tokens: row-range kernel, whole K per CTA, no workspace use
+    GemvRowsParams r = {};
+    r.xq = x_q;
+    r.scale = scale;
+    r.w_scale = w_scale;
+    r.y = y;
+    r.acc = acc;
+    r.N = N;
+    r.K = K;
+    r.M = (int)M;
+    r.NKB = (int)cdiv(K, kStageK);
+    r.units = (int)cdiv(N, 8);
+    r.xrow = r.NKB * kStageK;
+    CUtensorMap m64, m8;
+    if (bitnet_status s = encode_packed_map(&m64, packed, N, K, 128, kRowsGroup, CU_TENSOR_MAP_SWIZZLE_128B))
+      return s;
+    if (bitnet_status s = encode_packed_map(&m8, packed, N, K, 128, 8, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
+    const size_t smem = gemv_rows_smem_layout((int)M, r.xrow).bytes + 1024;
+    const int grid = std::min(d->sms, r.units);
+    auto k = M == 1 ? gemv_rows_kernel<1> : gemv_rows_kernel<2>;
+    if (set_smem(k, smem) != BITNET_OK) return BITNET_ERR_CUDA;
+    return launch(k, dim3(grid), dim3(kRowsThreads), smem, stream, m64, m8, r);
+  }
   CUtensorMap map;
   if (bitnet_status s = encode_packed_map(&map, packed, N, K, kStageRowBytes, kStageRows,
                                           CU_TENSOR_MAP_SWIZZLE_128B))
@@ -314,7 +339,7 @@ int bitnet_w2a8_gemv(const int8_t *x_q, const float *scale, int64_t M, const uin
 }
 
 size_t bitnet_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  if (M <= 0 || !shape_ok(N, K)) return 0;
+  if (M <= 0 || !shape_ok(N, K) || M > kMaxElems / K) return 0;
   return gemm_workspace_bytes(M, N, K);
 }
 
@@ -322,10 +347,65 @@ int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uin
                      const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc, void *workspace,
                      size_t workspace_bytes, cudaStream_t stream) {
   if (bitnet_status s = check_gemm_args(x_q, scale, M, packed, w_scale, N, K, y, workspace)) return s;
-  if (workspace_bytes < gemm_workspace_bytes(M, N, K)) return BITNET_ERR_WORKSPACE;
+  if (!aligned(acc, 4)) return BITNET_ERR_ALIGNMENT;
+  if (N > 0x7fffffff || K > 0x7fffffff || M > 0x7fffffff) return BITNET_ERR_SHAPE;
+  if (workspace_bytes < gemm_workspace_bytes(M, N, K) || !aligned(workspace, 256)) return BITNET_ERR_WORKSPACE;
   DeviceInfo *d;
   if (bitnet_status s = device_info(&d)) return s;
-  return gemm_launch(x_q, scale, M, packed, w_scale, N, K, y, acc, workspace, d->sms, stream);
+
+  const bool tc_ok = (K % 64 == 0) && K >= 512 && aligned(packed, 16) && aligned(x_q, 16);
+  if (!tc_ok) {
+    GemvParams p = {};
+    p.packed = packed;
+    p.xq = x_q;
+    p.scale = scale;
+    p.w_scale = w_scale;
+    p.y = y;
+    p.acc = acc;
+    p.N = N;
+    p.K = K;
+    p.M = (int)M;
+    const long long items = (long long)N * M;
+    const int blocks = (int)std::min<long long>(cdiv(items, 8), (long long)d->sms * 16);
+    return launch(gemv_generic_kernel, dim3(blocks), dim3(256), 0, stream, p);
+  }
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  uint32_t *xb = reinterpret_cast<uint32_t *>(ws);
+  int32_t *xsum = reinterpret_cast<int32_t *>(ws + gemm_xb_bytes(M, K));
+  float *fscale = reinterpret_cast<float *>(ws + gemm_xb_bytes(M, K) + (size_t)M * 4);
+
+  bitnet_status st = launch(gemm_prep_kernel, dim3((unsigned)M), dim3(256), 0, stream, x_q, scale, w_scale, K,
+                            xb, xsum, fscale);
+  if (st) return st;
+
+  CUtensorMap wmap, bmap;
+  if (bitnet_status s = encode_packed_map(&wmap, packed, N, K, 128, kGemmRows, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {kGemmKB, kGemmTok};
+    cuuint32_t estr[2] = {1, 1};
+    if (g_encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xb, dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return BITNET_ERR_CUDA;
+  }
+  GemmParams p = {};
+  p.y = y;
+  p.acc = acc;
+  p.xsum = xsum;
+  p.fscale = fscale;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.NRT = (int)cdiv(N, kGemmRows);
+  p.NTT = (int)cdiv(M, kGemmTok);
+  p.NKB = (int)cdiv(K, kGemmKB);
+  p.tiles = (long long)p.NRT * p.NTT;
+  const size_t smem = gemm_smem_layout().bytes + 1024;
+  if (set_smem(gemm_tc_kernel, smem) != BITNET_OK) return BITNET_ERR_CUDA;
+  const int grid = (int)std::min<long long>(d->sms, p.tiles);
+  return launch(gemm_tc_kernel, dim3(grid), dim3(kGemmThreads), smem, stream, wmap, bmap, p);
 }
 
 int bitnet_check_device_error(cudaStream_t stream) {

@@ -1,18 +1,400 @@
-// Prefill-path W2A8 ternary GEMM on tcgen05 tensor cores (in progress).
+// Prefill-path W2A8 ternary GEMM on the tcgen05 tensor cores.
+//
+// y[m, n] = (sum_k (code[n,k]-1) * x_q[m,k]) * (w_scale * s_m / 127): the
+// integer-domain matmul of BitNet 深度拆解 §3.1 with the dequantisation of
+// §2.3, for many tokens at once (the prefill counterpart of the decode GEMV).
+//
+// D (weight rows x tokens) = A (weight rows x K) * B (tokens x K)^T, one
+// 128 x 128 tile per CTA iteration, kind::f16 MMA with fp32 accumulators in
+// tensor memory:
+//   * A comes from TMEM.  Decoder warps read the packed codes (TMA, 128-byte
+//     swizzle) and turn each 2-bit field, masked in place inside a 16-bit
+//     lane, into an fp16 subnormal code * 4^i * 2^-24; tcgen05.st writes them
+//     straight into TMEM, so decoded weights never occupy shared memory.
+//   * B is the activation matrix prepared once per call by gemm_prep_kernel:
+//     x_q as fp16, scaled by 4^-i to match the weight encoding, in the same
+//     K order as the decoded weights.  TMA loads 128 x 64 tiles with 128-byte
+//     swizzle (the canonical K-major UMMA layout).
+//   * Every product is code * x * 2^-24 and every partial sum an integer
+//     multiple of 2^-24 below 2^22 * 2^-24, so fp32 accumulation is exact and
+//     D * 2^24 - sum_k x_q is the exact integer accumulator.
+//   * Two accumulators (256 TMEM columns) let the epilogue of one tile overlap
+//     the MMAs of the next.
+// Warp roles: 0 TMA producer, 1 TMEM owner + MMA issuer, 4-7 decoders,
+// 8-11 epilogue.  Every wait is bounded (kWaitLimitNs); on expiry the CTA
+// records the error, stops issuing work, drains what it issued, frees TMEM
+// and exits.
 #pragma once
 
 #include "common.cuh"
 
 namespace bitnet {
 
-inline size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  (void)N;
-  return (size_t)M * (size_t)K * 2 + (size_t)M * 4 + 1024;
+constexpr int kGemmThreads = 384;
+constexpr int kGemmRows = 128;   // weight rows per tile (MMA M)
+constexpr int kGemmTok = 128;    // tokens per tile (MMA N)
+constexpr int kGemmKB = 64;      // K per pipeline step (4 MMAs of K = 16)
+constexpr int kGemmStages = 6;   // B stages in smem == A buffers in TMEM
+constexpr int kGemmBStageBytes = kGemmTok * 128;
+constexpr int kGemmWStages = 2;  // packed-weight stages (128 rows x 512 K)
+constexpr int kGemmWStageBytes = kGemmRows * 128;
+constexpr int kGemmTmemCols = 512;
+constexpr int kGemmAccCol = 0;   // two accumulators: columns [0, 256)
+constexpr int kGemmACol = 256;   // A buffers: columns [256, 256 + 6 * 32)
+
+struct GemmParams {
+  float *y;
+  int32_t *acc;
+  const int32_t *xsum;  // [M]
+  const float *fscale;  // [M] = w_scale * s_m / 127
+  int64_t M, N, K;
+  int NRT, NTT, NKB;
+  long long tiles;
+};
+
+struct GemmSmem {
+  int bstage, wstage, bars, tmem_slot, flags, bytes;
+};
+
+__host__ __device__ constexpr GemmSmem gemm_smem_layout() {
+  return GemmSmem{0, kGemmStages * kGemmBStageBytes,
+                  kGemmStages * kGemmBStageBytes + kGemmWStages * kGemmWStageBytes,
+                  kGemmStages * kGemmBStageBytes + kGemmWStages * kGemmWStageBytes + 256,
+                  kGemmStages * kGemmBStageBytes + kGemmWStages * kGemmWStageBytes + 272,
+                  kGemmStages * kGemmBStageBytes + kGemmWStages * kGemmWStageBytes + 288};
 }
 
-inline int gemm_launch(const int8_t *, const float *, int64_t, const uint8_t *, const float *, int64_t, int64_t,
-                       float *, int32_t *, void *, int, cudaStream_t) {
-  return 4;  // BITNET_ERR_UNSUPPORTED until the tcgen05 kernel lands
+// ---------------------------------------------------------- tcgen05 PTX --
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16, fp32 accumulate.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (rows of 128 bytes), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor: kind::f16, A = B = f16, D = f32, both K-major.
+__host__ __device__ constexpr uint32_t gemm_idesc(int m, int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// --------------------------------------------------------------- prep --
+
+// x_q int8 [M, K] -> fp16 B matrix [M, K] (per 16-K group, element 2i+h is
+// x[16q + 8h + i] * 4^-e(i), e = {0,1,2,3,4,5,0,1}), per-token sum of x_q and
+// the per-token output scale w_scale * s_m / 127.  One CTA per token.
+__global__ void __launch_bounds__(256) gemm_prep_kernel(const int8_t *__restrict__ xq, const float *__restrict__ scale,
+                                                        const float *__restrict__ w_scale, int64_t K,
+                                                        uint32_t *__restrict__ xb, int32_t *__restrict__ xsum,
+                                                        float *__restrict__ fscale) {
+  pdl_wait_prior_grid();
+  pdl_launch_dependents();
+  __shared__ int red[8];
+  const int64_t m = blockIdx.x;
+  const int8_t *row = xq + m * K;
+  uint32_t *out = xb + m * (K / 2);
+  int sum = 0;
+  for (int64_t q = threadIdx.x; q < K / 16; q += 256) {
+    const int4 u = *reinterpret_cast<const int4 *>(row + q * 16);
+    int8_t v[16];
+    memcpy(v, &u, 16);
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = i < 6 ? i : i - 6;
+      const float sc = 1.0f / (float)(1 << (2 * e));
+      h[i] = (uint32_t)__half_as_ushort(__float2half_rn((float)v[i] * sc)) |
+             ((uint32_t)__half_as_ushort(__float2half_rn((float)v[8 + i] * sc)) << 16);
+      sum += v[i] + v[8 + i];
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(out + q * 8);
+    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int w = 0; w < 8; ++w) t += red[w];
+    xsum[m] = t;
+    fscale[m] = __fdiv_rn(__fmul_rn(__ldg(w_scale), __ldg(scale + m)), 127.0f);
+  }
+}
+
+// --------------------------------------------------------------- main --
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap bmap,
+                   const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr GemmSmem L = gemm_smem_layout();
+  uint64_t *bfull = reinterpret_cast<uint64_t *>(smem + L.bars);  // [6] TMA -> MMA
+  uint64_t *kempty = bfull + kGemmStages;                            // [6] MMA done -> producer, decoders
+  uint64_t *afull = kempty + kGemmStages;                            // [6] decoders -> MMA
+  uint64_t *wfull = afull + kGemmStages;                             // [2] TMA -> decoders
+  uint64_t *wempty = wfull + kGemmWStages;                           // [2] decoders -> producer
+  uint64_t *accfull = wempty + kGemmWStages;                         // [2] MMA -> epilogue
+  uint64_t *accempty = accfull + 2;                                  // [2] epilogue -> MMA
+  uint64_t *drain = accempty + 2;                                    // [1] final MMA completion
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.tmem_slot);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flags);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kGemmStages; ++i) {
+      mbar_init(&bfull[i], 1);
+      mbar_init(&kempty[i], 1);
+      mbar_init(&afull[i], 4);
+    }
+    for (int i = 0; i < kGemmWStages; ++i) {
+      mbar_init(&wfull[i], 1);
+      mbar_init(&wempty[i], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accfull[i], 1);
+      mbar_init(&accempty[i], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kGemmTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto wait = [&](uint64_t *bar, uint32_t parity) {
+    if (*abort_flag) return;
+    if (!mbar_wait(bar, parity)) {
+      raise_device_error(kDevErrTimeout);
+      *abort_flag = 1;
+    }
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------- TMA producer --
+    if (lane == 0) {
+      prefetch_tensormap(&wmap);
+      prefetch_tensormap(&bmap);
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_b = l2_policy_evict_last();
+      long long c = 0, wc = 0;
+      bool waited_prior = false;
+      for (long long t = blockIdx.x; t < p.tiles && !*abort_flag; t += gridDim.x) {
+        const int rt = (int)(t % p.NRT), tt = (int)(t / p.NRT);
+        for (int kb = 0; kb < p.NKB && !*abort_flag; ++kb, ++c) {
+          if ((kb & 7) == 0) {
+            const int ws = (int)(wc % kGemmWStages);
+            if (wc >= kGemmWStages) wait(&wempty[ws], (uint32_t)(((wc / kGemmWStages) - 1) & 1));
+            if (*abort_flag) break;
+            mbar_arrive_expect_tx(&wfull[ws], kGemmWStageBytes);
+            tma_load_2d(smem + L.wstage + ws * kGemmWStageBytes, &wmap, &wfull[ws], (kb >> 3) * 128,
+                        rt * kGemmRows, pol_w);
+            ++wc;
+          }
+          if (!waited_prior) {  // activations come from the previous kernel
+            pdl_wait_prior_grid();
+            waited_prior = true;
+          }
+          const int s = (int)(c % kGemmStages);
+          if (c >= kGemmStages) wait(&kempty[s], (uint32_t)(((c / kGemmStages) - 1) & 1));
+          if (*abort_flag) break;
+          mbar_arrive_expect_tx(&bfull[s], kGemmBStageBytes);
+          tma_load_2d(smem + L.bstage + s * kGemmBStageBytes, &bmap, &bfull[s], kb * kGemmKB, tt * kGemmTok,
+                      pol_b);
+        }
+      }
+      if (!waited_prior) pdl_wait_prior_grid();
+      if (*abort_flag) {
+        // drain: wait (bounded) for every copy this thread may have in flight
+        for (long long j = (c > kGemmStages ? c - kGemmStages : 0); j < c; ++j)
+          mbar_wait(&bfull[j % kGemmStages], (uint32_t)((j / kGemmStages) & 1));
+        for (long long j = (wc > kGemmWStages ? wc - kGemmWStages : 0); j < wc; ++j)
+          mbar_wait(&wfull[j % kGemmWStages], (uint32_t)((j / kGemmWStages) & 1));
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      pdl_wait_prior_grid();
+      const uint32_t idesc = gemm_idesc(kGemmRows, kGemmTok);
+      const uint32_t bbase = smem_u32(smem + L.bstage);
+      long long c = 0, tc = 0;
+      for (long long t = blockIdx.x; t < p.tiles && !*abort_flag; t += gridDim.x, ++tc) {
+        const int a = (int)(tc & 1);
+        if (tc >= 2) wait(&accempty[a], (uint32_t)(((tc >> 1) - 1) & 1));
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + kGemmAccCol + a * kGemmTok;
+        for (int kb = 0; kb < p.NKB && !*abort_flag; ++kb, ++c) {
+          const int s = (int)(c % kGemmStages);
+          const uint32_t par = (uint32_t)((c / kGemmStages) & 1);
+          wait(&bfull[s], par);
+          wait(&afull[s], par);
+          if (*abort_flag) break;
+          tc_fence_after();
+          const uint64_t bdesc = smem_desc_sw128(bbase + s * kGemmBStageBytes);
+          const uint32_t a_tmem = tmem + kGemmACol + s * 32;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_ts(d_tmem, a_tmem + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+          tc_commit(&kempty[s]);
+        }
+        tc_commit(&accfull[a]);
+      }
+      // every MMA this thread issued has completed once `drain` flips
+      tc_commit(drain);
+      mbar_wait(drain, 0);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------------------------------------------------- decoders --
+    // tcgen05.st is warp-collective: the abort decision is made warp-uniform.
+    pdl_wait_prior_grid();
+    const int quad = warp & 3, row = quad * 32 + lane;
+    const uint32_t wbase = smem_u32(smem + L.wstage);
+    long long c = 0, wc = 0;
+    bool stop = false;
+    for (long long t = blockIdx.x; t < p.tiles && !stop; t += gridDim.x) {
+      for (int kb = 0; kb < p.NKB; ++kb, ++c) {
+        const int ws = (int)(wc % kGemmWStages);
+        if ((kb & 7) == 0) wait(&wfull[ws], (uint32_t)((wc / kGemmWStages) & 1));
+        const int s = (int)(c % kGemmStages);
+        if (c >= kGemmStages) wait(&kempty[s], (uint32_t)(((c / kGemmStages) - 1) & 1));
+        if (__any_sync(0xffffffffu, *abort_flag)) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        const int chunk = kb & 7;
+        const uint4 v = lds_u128(wbase + ws * kGemmWStageBytes + row * 128 + (((chunk ^ (row & 7)) & 7) << 4));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t h[32];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t hs = w[u] >> 12;
+#pragma unroll
+          for (int i = 0; i < 6; ++i) h[8 * u + i] = w[u] & (0x00030003u << (2 * i));
+          h[8 * u + 6] = hs & 0x00030003u;
+          h[8 * u + 7] = hs & 0x000C000Cu;
+        }
+        tmem_st_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + kGemmACol + s * 32, h);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull[s]);
+        if (chunk == 7 || kb == p.NKB - 1) {
+          if (lane == 0) mbar_arrive(&wempty[ws]);
+          ++wc;
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ---------------------------------------------------------- epilogue --
+    pdl_wait_prior_grid();
+    const int quad = warp & 3, row = quad * 32 + lane;
+    long long tc = 0;
+    for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x, ++tc) {
+      const int rt = (int)(t % p.NRT), tt = (int)(t / p.NRT);
+      const int a = (int)(tc & 1);
+      wait(&accfull[a], (uint32_t)((tc >> 1) & 1));
+      if (__any_sync(0xffffffffu, *abort_flag)) break;  // tcgen05.ld is warp-collective
+      tc_fence_after();
+      const int64_t n = (int64_t)rt * kGemmRows + row;
+#pragma unroll 1
+      for (int cb = 0; cb < kGemmTok / 32; ++cb) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + kGemmAccCol + a * kGemmTok + cb * 32, r);
+        const int64_t tok0 = (int64_t)tt * kGemmTok + cb * 32;
+        if (n < p.N) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int64_t tok = tok0 + j;
+            if (tok < p.M) {
+              const int32_t v = __float2int_rn(__uint_as_float(r[j]) * 16777216.0f) - __ldg(p.xsum + tok);
+              if (p.acc) p.acc[tok * p.N + n] = v;
+              p.y[tok * p.N + n] = __fmul_rn((float)v, __ldg(p.fscale + tok));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accempty[a]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kGemmTmemCols);
+  }
+}
+
+// ------------------------------------------------------------- host side --
+
+inline size_t gemm_xb_bytes(int64_t M, int64_t K) { return (((size_t)M * (size_t)K * 2) + 1023) & ~(size_t)1023; }
+
+inline size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  (void)N;
+  return gemm_xb_bytes(M, K) + (((size_t)M * 8 + 255) & ~(size_t)255) + 1024;
 }
 
 }  // namespace bitnet

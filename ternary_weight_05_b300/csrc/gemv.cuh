@@ -104,6 +104,18 @@ __device__ __forceinline__ StageCoord stage_coord(const GemvParams &p, long long
   return c;
 }
 
+// Next stage in (slice, row tile, K-block) order without dividing.
+__device__ __forceinline__ void stage_advance(const GemvParams &p, StageCoord &c) {
+  if (++c.kbl == c.nk) {
+    c.kbl = 0;
+    if (++c.r == p.NR) {
+      c.r = 0;
+      ++c.s;
+      c.nk = min(p.KBS, p.NKB - c.s * p.KBS);
+    }
+  }
+}
+
 __device__ __forceinline__ void consumer_sync() { named_barrier_sync(kGemvConsumerBar, kGemvConsumers); }
 
 // Activation-slice loader.  For slice s, K range [s*KBS*512, ...), writes the
@@ -424,7 +436,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 
   const long long g0 = p.total * blockIdx.x / gridDim.x;
   const long long g1 = p.total * (blockIdx.x + 1) / gridDim.x;
-  const long long count = g1 - g0;
+  const int count = (int)(g1 - g0);
   const int tid = threadIdx.x, lane = tid & 31;
 
   if (tid == 0) {
@@ -442,14 +454,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   // Thread 0 is also the TMA producer.  The weights do not depend on the
   // previous kernel, so the first stages are requested before waiting on it.
   uint64_t policy = 0;
-  auto issue = [&](long long j) {
-    const int slot = (int)(j % kGemvStages);
-    const StageCoord c = stage_coord(p, g0 + j);
+  StageCoord pc = stage_coord(p, g0);  // producer position
+  auto issue = [&](int j) {
+    const int slot = j % kGemvStages;
     mbar_arrive_expect_tx(&full[slot], kStageBytes);
-    tma_load_2d(smem + L.ring + slot * kStageBytes, &wmap, &full[slot], (c.s * p.KBS + c.kbl) * kStageRowBytes,
-                c.r * kStageRows, policy);
+    tma_load_2d(smem + L.ring + slot * kStageBytes, &wmap, &full[slot], (pc.s * p.KBS + pc.kbl) * kStageRowBytes,
+                pc.r * kStageRows, policy);
+    stage_advance(p, pc);
   };
-  long long issued = 0;
+  int issued = 0;
   if (tid == 0) {
     prefetch_tensormap(&wmap);
     policy = l2_policy_evict_first();
@@ -464,8 +477,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   const uint32_t ring = smem_u32(smem + L.ring);
   const uint32_t xs = smem_u32(smem + L.xbuf);
   int cur_s = -1, cur_r = -1, seg_kb0 = 0;
-  for (long long it = 0; it < count; ++it) {
-    const StageCoord c = stage_coord(p, g0 + it);
+  StageCoord c = stage_coord(p, g0);
+  for (int it = 0; it < count; ++it, stage_advance(p, c)) {
     if (c.s != cur_s) {
       gemv_load_x_slice<Policy::kHmma>(p, c.s, smem + L.xbuf, xsum);
       cur_s = c.s;
@@ -474,7 +487,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       cur_r = c.r;
       seg_kb0 = c.kbl;
     }
-    const int slot = (int)(it % kGemvStages);
+    const int slot = it % kGemvStages;
     // After a timeout every thread keeps walking the same stages without
     // waiting, so all warps reach the same named barriers; the results are
     // then meaningless and the device error word says so.
@@ -503,7 +516,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   }
   // Leave no bulk copy in flight (only possible after a timeout).
   if (tid == 0 && flags[0]) {
-    for (long long j = (issued > kGemvStages ? issued - kGemvStages : 0); j < issued; ++j)
+    for (int j = (issued > kGemvStages ? issued - kGemvStages : 0); j < issued; ++j)
       mbar_wait(&full[j % kGemvStages], (uint32_t)((j / kGemvStages) & 1));
   }
 }

@@ -77,8 +77,10 @@ def weights_torch(N: int, K: int, dist: str, scale: float, seed: int, device):
     if dist == "normal":
         return torch.randn((N, K), generator=g, device=device, dtype=torch.float32) * scale
     if dist == "laplace":
-        u = torch.rand((N, K), generator=g, device=device, dtype=torch.float32) - 0.5
-        return -scale * torch.sign(u) * torch.log1p(-2.0 * u.abs())
+        # difference of two Exp(1) draws; 1 - U lies in (0, 1], so the logs are finite
+        e1 = -torch.log1p(-torch.rand((N, K), generator=g, device=device, dtype=torch.float32))
+        e2 = -torch.log1p(-torch.rand((N, K), generator=g, device=device, dtype=torch.float32))
+        return scale * (e1 - e2)
     raise ValueError(dist)
 
 
