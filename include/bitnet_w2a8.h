@@ -10,7 +10,9 @@
  * Conventions shared by every call
  *   - Device pointers are CUDA device (or managed) memory owned by the caller;
  *     host pointers are named as such.  The library allocates no device
- *     memory: scratch space is passed in as a caller-owned workspace.
+ *     memory: scratch space is passed in as a caller-owned workspace (the
+ *     one exception is the fixed array of bitnet_w2a8_gemv_static_scratch,
+ *     part of the loaded module, not a runtime allocation).
  *   - Every call validates its arguments on the host before enqueuing
  *     anything.  On a non-zero status nothing has been enqueued.
  *   - Calls are asynchronous and stream-ordered on `stream` (0 = legacy
@@ -42,7 +44,8 @@ typedef enum {
   BITNET_ERR_UNSUPPORTED = 4, /* no sm_103 device / kernel image for this device */
   BITNET_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
   BITNET_ERR_TIMEOUT = 6,     /* a device-side bounded wait expired */
-  BITNET_ERR_WORKSPACE = 7    /* workspace null or smaller than required */
+  BITNET_ERR_WORKSPACE = 7,   /* workspace null or smaller than required */
+  BITNET_ERR_TOO_LARGE = 8    /* needs more scratch than the library's fixed array holds */
 } bitnet_status;
 
 /* Element type of floating-point inputs. */
@@ -139,6 +142,43 @@ size_t bitnet_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
                      const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc,
                      void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of the fixed device array behind bitnet_w2a8_gemv_static_scratch. */
+#define BITNET_GEMV_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
+
+/*
+ * bitnet_w2a8_gemv_static_scratch -- bitnet_w2a8_gemv for callers that cannot
+ * allocate device memory.  No page counterpart: this is a packaging variant of
+ * the decode GEMV above, not a separate step of the method.
+ *
+ * Some callers may not call cudaMalloc at all: plugins whose host framework
+ * owns every device allocation, runtimes that pre-plan a fixed memory budget,
+ * or code that runs where an allocation could block or fail.  This entry
+ * point takes the same arguments as bitnet_w2a8_gemv minus the workspace and
+ * computes the same result (same kernels, same dispatch).  Its scratch is a
+ * 4 MiB array compiled into the library (BITNET_GEMV_STATIC_SCRATCH_BYTES);
+ * every GPU that loads the library holds that array until the process exits.
+ * The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
+ *
+ *   - Limit: a shape whose bitnet_gemv_workspace_bytes(M, N, K) exceeds
+ *     BITNET_GEMV_STATIC_SCRATCH_BYTES is rejected with BITNET_ERR_TOO_LARGE
+ *     (nothing enqueued).  For example M=16 fits N up to ~65k rows, M=64 up
+ *     to ~16k.
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress, with that device current) and caches it.
+ *     Make that first call outside any stream capture.
+ *   - Sharing: every call, on every stream, uses the same array.  The call
+ *     zeroes the part it needs (cudaMemsetAsync on `stream`) before the
+ *     kernel, so stale contents from an earlier call do not matter, but two
+ *     calls that can overlap on the GPU (different streams, no ordering
+ *     between them) race on the array and give wrong results.  Order them on
+ *     one stream, or use bitnet_w2a8_gemv with separate workspaces.
+ * Errors: as bitnet_w2a8_gemv, plus TOO_LARGE; WORKSPACE never occurs.
+ */
+int bitnet_w2a8_gemv_static_scratch(const int8_t *x_q, const float *scale, int64_t M,
+                                    const uint8_t *packed, const float *w_scale, int64_t N,
+                                    int64_t K, float *y, int32_t *acc, cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device error word of the

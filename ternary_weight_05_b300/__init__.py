@@ -19,10 +19,11 @@ from ._lib import BitnetError
 __all__ = [
     "BitnetError", "pack_weights", "quant_act", "w2a8_gemv", "w2a8_gemm", "bitlinear",
     "pack_workspace_bytes", "gemv_workspace_bytes", "gemm_workspace_bytes", "check_device_error",
-    "set_pdl", "GEMV_MAX_M", "library_path",
+    "set_pdl", "GEMV_MAX_M", "library_path", "w2a8_gemv_static_scratch", "GEMV_STATIC_SCRATCH_BYTES",
 ]
 
 GEMV_MAX_M = 64
+GEMV_STATIC_SCRATCH_BYTES = 4 << 20
 F32, BF16 = 0, 1
 library_path = _lib.LIB_PATH
 
@@ -159,6 +160,26 @@ def w2a8_gemm(x_q, scale, packed, w_scale, N: int, K: int, want_acc: bool = Fals
     """Prefill GEMM (any M): y [M, N] fp32 (and the exact int32 acc if asked)."""
     return _matmul("bitnet_w2a8_gemm", _L().bitnet_gemm_workspace_bytes, "gemm", x_q, scale, packed, w_scale, N, K,
                    want_acc, out, workspace)
+
+
+def w2a8_gemv_static_scratch(x_q, scale, packed, w_scale, N: int, K: int, want_acc: bool = False, out=None):
+    """Decode GEMV like w2a8_gemv, for callers that cannot allocate device
+    scratch: the library's fixed 4 MiB device array is used instead of a
+    workspace (shapes that need more raise BitnetError TOO_LARGE).  Calls
+    that may overlap on the GPU share that array and must not run
+    concurrently.  The output tensors are still allocated here by torch
+    unless `out` is given."""
+    for t, nm in ((x_q, "x_q"), (scale, "scale"), (packed, "packed"), (w_scale, "w_scale")):
+        _dev(t, nm)
+    M = x_q.shape[0]
+    dev = x_q.device
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=dev)
+    acc = torch.empty((M, N), dtype=torch.int32, device=dev) if want_acc else None
+    st = _L().bitnet_w2a8_gemv_static_scratch(x_q.data_ptr(), scale.data_ptr(), M, packed.data_ptr(),
+                                              w_scale.data_ptr(), N, K, y.data_ptr(),
+                                              acc.data_ptr() if acc is not None else None, _stream(dev))
+    _lib.check("bitnet_w2a8_gemv_static_scratch", st)
+    return (y, acc) if want_acc else y
 
 
 def bitlinear(x: torch.Tensor, packed: torch.Tensor, beta: torch.Tensor, N: int, K: int):

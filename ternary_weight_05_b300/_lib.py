@@ -25,11 +25,13 @@ SIGNATURES = {
     "bitnet_gemm_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "bitnet_w2a8_gemm": (_i, [_p, _p, _i64, _p, _p, _i64, _i64, _p, _p, _p, _sz, _p]),
     "bitnet_check_device_error": (_i, [_p]),
+    "bitnet_w2a8_gemv_static_scratch": (_i, [_p, _p, _i64, _p, _p, _i64, _i64, _p, _p, _p]),
 }
 
 STATUS = {
     0: "BITNET_OK", 1: "BITNET_ERR_INVALID_ARG", 2: "BITNET_ERR_SHAPE", 3: "BITNET_ERR_ALIGNMENT",
     4: "BITNET_ERR_UNSUPPORTED", 5: "BITNET_ERR_CUDA", 6: "BITNET_ERR_TIMEOUT", 7: "BITNET_ERR_WORKSPACE",
+    8: "BITNET_ERR_TOO_LARGE",
 }
 
 _lib = None

@@ -20,6 +20,10 @@
 
 using namespace bitnet;
 
+// Scratch of bitnet_w2a8_gemv_static_scratch: a fixed array in the module
+// (zero-initialised at load; every device that loads the library holds it).
+static __device__ __align__(256) uint8_t g_gemv_static_scratch[BITNET_GEMV_STATIC_SCRATCH_BYTES];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -163,6 +167,25 @@ bitnet_status check_gemm_args(const int8_t *x_q, const float *scale, int64_t M, 
   return BITNET_OK;
 }
 
+// Device address of g_gemv_static_scratch per device, looked up once.
+void *g_static_scratch_addr[kMaxDevices];
+
+// Any non-null pointer: check_gemm_args only tests the workspace for null.
+void *const g_static_scratch_dummy = reinterpret_cast<void *>(uintptr_t(256));
+
+bitnet_status static_scratch_address(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BITNET_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_static_scratch_addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_gemv_static_scratch) != cudaSuccess || p == nullptr) return BITNET_ERR_CUDA;
+    g_static_scratch_addr[dev] = p;
+  }
+  *out = g_static_scratch_addr[dev];
+  return BITNET_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -177,6 +200,7 @@ const char *bitnet_status_string(int status) {
     case BITNET_ERR_CUDA: return "BITNET_ERR_CUDA";
     case BITNET_ERR_TIMEOUT: return "BITNET_ERR_TIMEOUT";
     case BITNET_ERR_WORKSPACE: return "BITNET_ERR_WORKSPACE";
+    case BITNET_ERR_TOO_LARGE: return "BITNET_ERR_TOO_LARGE";
     default: return "BITNET_ERR_UNKNOWN";
   }
 }
@@ -406,6 +430,35 @@ int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uin
   if (set_smem(gemm_tc_kernel, smem) != BITNET_OK) return BITNET_ERR_CUDA;
   const int grid = (int)std::min<long long>(d->sms, p.tiles);
   return launch(gemm_tc_kernel, dim3(grid), dim3(kGemmThreads), smem, stream, wmap, bmap, p);
+}
+
+// Decode GEMV whose scratch is the file-scope array g_gemv_static_scratch instead of a
+// caller workspace, for callers that cannot allocate device memory.  The
+// array is part of the loaded module: each device that loads the library
+// holds it until exit.  In host code `g_gemv_static_scratch` is only a
+// host-side stand-in for the symbol; its device address comes from
+// cudaGetSymbolAddress, looked up once per device (with that device current)
+// on the first call there.
+int bitnet_w2a8_gemv_static_scratch(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
+                                    const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc,
+                                    cudaStream_t stream) {
+  // Validate everything bitnet_w2a8_gemv checks before the memset below is
+  // enqueued, so that a rejected call enqueues nothing.
+  if (bitnet_status s = check_gemm_args(x_q, scale, M, packed, w_scale, N, K, y, g_static_scratch_dummy))
+    return s;
+  if (!aligned(acc, 4)) return BITNET_ERR_ALIGNMENT;
+  if (M > BITNET_GEMV_MAX_M || N > 0x7fffffff || K > 0x7fffffff) return BITNET_ERR_SHAPE;
+  const size_t need = bitnet_gemv_workspace_bytes(M, N, K);
+  if (need == 0) return BITNET_ERR_SHAPE;
+  if (need > BITNET_GEMV_STATIC_SCRATCH_BYTES) return BITNET_ERR_TOO_LARGE;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
+  void *scratch = nullptr;
+  if (bitnet_status s = static_scratch_address(&scratch)) return s;
+  // The array keeps whatever the previous call (or an aborted one) left:
+  // the GEMV needs its scratch zero-filled on entry.
+  if (cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) return BITNET_ERR_CUDA;
+  return bitnet_w2a8_gemv(x_q, scale, M, packed, w_scale, N, K, y, acc, scratch, need, stream);
 }
 
 int bitnet_check_device_error(cudaStream_t stream) {
