@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--M", type=int, default=None, help="tokens (decode workloads)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="decode step as quant_act + w2a8_gemv (two calls) instead of the fused bitlinear call")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -194,16 +196,28 @@ def run_native(args):
         return run_prefill(args, dev, rank, world, bf16_peak, peak_src)
 
     wl, stack, M = build_stack(args, dev, rank)
-    max_ws = max(tw.gemv_workspace_bytes(M, e["L"].N, e["L"].K) for e in stack)
+    fused = not args.unfused
+    max_ws = max(max(tw.gemv_workspace_bytes(M, e["L"].N, e["L"].K), tw.bitlinear_workspace_bytes(M, e["L"].N,
+                                                                                                 e["L"].K))
+                 for e in stack)
     ws = torch.zeros(max_ws, dtype=torch.uint8, device=dev)
     wbytes = sum(e["L"].N * e["L"].K // 4 for e in stack)
-    # algorithmic bytes of the GEMV: packed weights + x_q + scales + y
-    gemv_bytes = sum(e["L"].N * e["L"].K // 4 + M * e["L"].K + 4 * M + 4 * M * e["L"].N + 4 for e in stack)
+    xes = stack[0]["x"].element_size()
+    if fused:
+        # fused BitLinear kernel: packed weights + x (bf16/fp32) + w_scale + y
+        gemv_bytes = sum(e["L"].N * e["L"].K // 4 + xes * M * e["L"].K + 4 + 4 * M * e["L"].N for e in stack)
+    else:
+        # GEMV: packed weights + x_q + scales + w_scale + y
+        gemv_bytes = sum(e["L"].N * e["L"].K // 4 + M * e["L"].K + 4 * M + 4 + 4 * M * e["L"].N for e in stack)
 
     def step():
         for e in stack:
-            tw.quant_act(e["x"], out=(e["xq"], e["s"]))
-            tw.w2a8_gemv(e["xq"], e["s"], e["packed"], e["beta"], e["L"].N, e["L"].K, out=e["y"], workspace=ws)
+            if fused:
+                tw.bitlinear(e["x"], e["packed"], e["beta"], e["L"].N, e["L"].K, out=e["y"], workspace=ws)
+            else:
+                tw.quant_act(e["x"], out=(e["xq"], e["s"]))
+                tw.w2a8_gemv(e["xq"], e["s"], e["packed"], e["beta"], e["L"].N, e["L"].K, out=e["y"],
+                             workspace=ws)
 
     tw.set_pdl(not args.no_pdl)
     stream = torch.cuda.Stream(dev)
@@ -235,12 +249,16 @@ def run_native(args):
 
         # GEMV kernel duration: a graph holding only the GEMV launches of the
         # stack (same inputs, same launch configuration, weights colder than
-        # L2 since the stack exceeds it), replayed between two events.
+        # L2 since the stack exceeds it), replayed between two events.  In
+        # the fused form the GEMV kernel is the whole step.
         gemv_graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gemv_graph, stream=stream):
             for e in stack:
-                tw.w2a8_gemv(e["xq"], e["s"], e["packed"], e["beta"], e["L"].N, e["L"].K, out=e["y"],
-                             workspace=ws)
+                if fused:
+                    tw.bitlinear(e["x"], e["packed"], e["beta"], e["L"].N, e["L"].K, out=e["y"], workspace=ws)
+                else:
+                    tw.w2a8_gemv(e["xq"], e["s"], e["packed"], e["beta"], e["L"].N, e["L"].K, out=e["y"],
+                                 workspace=ws)
         for _ in range(2):
             gemv_graph.replay()
         n_meas = max(3, args.steps)
@@ -285,20 +303,25 @@ def run_native(args):
     value = world * wbytes / (ms_step * 1e-3) / 1e9
     e2e_val = world * wbytes * args.steps / e2e_s / 1e9
     achieved = gemv_bytes * n_meas / (gemv_ms * 1e-3) / 1e9
+    # kernels per BitLinear: fused M <= 2: 1; fused M >= 3: prep + tensor-core GEMV;
+    # unfused: quant_act (+ prep for M >= 3) + GEMV
+    per_layer = (1 if M <= 2 else 2) if fused else (2 if M <= 2 else 3)
+    kname = ("gemv_rows_kernel" if M <= 2 else "gemv_tc_kernel") + (" (fused quant)" if fused else "")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded, weights and activations drawn on device)",
         "config": {"workload": f"{wl.name}: {wl.description}", "layers_in_stack": len(stack), "M": M,
+                   "step": "fused bitlinear per layer" if fused else "quant_act + w2a8_gemv per layer",
                    "packed_weight_bytes_per_step": wbytes, "graph": not args.no_graph, "pdl": not args.no_pdl,
                    "l2": "inputs larger than L2 (packed stack %.0f MB > 126 MB L2)" % (wbytes / 1e6),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": None,
-                     "kernel": "gemv_rows_kernel" if M <= 2 else "gemv_tma_kernel", "peak_source": peak_src,
+                     "kernel": kname, "peak_source": peak_src,
                      "launches_timed": gemv_launches, "avg_launch_us": round(1e3 * gemv_ms / gemv_launches, 3)},
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * len(stack) * args.steps,
+        "gpu_launches": per_layer * len(stack) * args.steps,
         "gemv_only_GBps": round(wbytes * n_meas / (gemv_ms * 1e-3) / 1e9, 2),
         "clocks": clk,
     }
@@ -330,7 +353,8 @@ def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
                          xq=torch.empty((M, L.K), dtype=torch.int8, device=dev),
                          s=torch.empty(M, dtype=torch.float32, device=dev),
                          y=torch.empty((M, L.N), dtype=torch.float32, device=dev),
-                         ws=torch.empty(tw.gemm_workspace_bytes(M, L.N, L.K), dtype=torch.uint8, device=dev)))
+                         ws=torch.empty(tw.gemm_workspace_bytes(M, L.N, L.K), dtype=torch.uint8, device=dev),
+                         wsb=torch.zeros(tw.bitlinear_workspace_bytes(M, L.N, L.K), dtype=torch.uint8, device=dev)))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     flops = sum(2.0 * M * m["L"].N * m["L"].K for m in mats)
     tw.set_pdl(not args.no_pdl)
@@ -338,9 +362,12 @@ def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
     with torch.cuda.stream(stream):
         def step():
             for m in mats:
-                tw.quant_act(m["x"], out=(m["xq"], m["s"]))
-                tw.w2a8_gemm(m["xq"], m["s"], m["packed"], m["beta"], m["L"].N, m["L"].K, out=m["y"],
-                             workspace=m["ws"])
+                if args.unfused:
+                    tw.quant_act(m["x"], out=(m["xq"], m["s"]))
+                    tw.w2a8_gemm(m["xq"], m["s"], m["packed"], m["beta"], m["L"].N, m["L"].K, out=m["y"],
+                                 workspace=m["ws"])
+                else:
+                    tw.bitlinear(m["x"], m["packed"], m["beta"], m["L"].N, m["L"].K, out=m["y"], workspace=m["wsb"])
 
         def gemm_only():
             for m in mats:
@@ -363,6 +390,8 @@ def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
             step()
             b.record(stream)
             spans.append((a, b))
+        for m in mats:  # int8 activations for the GEMM-only timing
+            tw.quant_act(m["x"], out=(m["xq"], m["s"]))
         for _ in range(args.steps):
             flush.fill_(2)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -404,6 +433,7 @@ def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
         "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded, drawn on device)",
         "config": {"workload": f"{wl.name}: {wl.description}", "M": M,
                    "matrices": [f"{m['L'].N}x{m['L'].K}" for m in mats], "l2": "flushed between steps (256 MB)",
+                   "step": "quant_act + w2a8_gemm per matrix" if args.unfused else "fused bitlinear per matrix",
                    "pdl": not args.no_pdl, "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16_peak, "unit": "TFLOP/s",
                      "frac": round(achieved / bf16_peak, 4), "traffic": None, "kernel": "gemm_tc_kernel (+prep)",
@@ -411,7 +441,7 @@ def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TOPS",
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hx),
                 "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hy)},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (6 if args.unfused else 4) * args.steps,
         "clocks": clk,
     }
     if rank == 0:

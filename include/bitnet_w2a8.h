@@ -117,9 +117,9 @@ size_t bitnet_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   y        device, [M, N] float out: y = acc * (w_scale * s_m / 127) in fp32.
  *   acc      device, [M, N] int32 out or NULL: acc = sum_k (code-1) * x_q,
  *            exact.
- *   workspace device, >= bitnet_gemv_workspace_bytes(M, N, K) bytes.  Must be
- *            zero-filled before its first use; every successful call leaves it
- *            zero-filled again (after BITNET_ERR_TIMEOUT, zero it again).
+ *   workspace device, >= bitnet_gemv_workspace_bytes(M, N, K) bytes, 16-byte
+ *            aligned, any contents: the call zeroes, in stream order, the
+ *            part it accumulates into.
  * Packed codes equal to 3 never come out of bitnet_pack_weights; the GEMV
  * does not define a result for them.
  * Errors: INVALID_ARG, SHAPE (M outside 1..64, N, K <= 0, K % 4 != 0),
@@ -141,6 +141,33 @@ size_t bitnet_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
  */
 int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
                      const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc,
+                     void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes bitnet_bitlinear needs. */
+size_t bitnet_bitlinear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * bitnet_bitlinear -- the whole BitLinear forward of [Deep-dive] §3.1 in one
+ * call: per-token absmax int8 quantisation of x (§2.2), the ternary integer
+ * product and the rescale y = acc * w_scale * s_m / 127 (§2.3).  The
+ * quantisation is fused into the matmul's prologue ([Deep-dive] §5.3 names
+ * this fusion as a key optimisation): for M <= 2 one kernel, otherwise one
+ * kernel that quantises straight into the tensor-core operand layout plus the
+ * GEMV (M <= 64) or GEMM kernel.  Results are bit-identical to
+ * bitnet_quant_act followed by bitnet_w2a8_gemv / bitnet_w2a8_gemm.
+ *
+ *   x        device, [M, K] row-major, BITNET_F32 or BITNET_BF16.
+ *   packed, w_scale, N, K, y, acc: as bitnet_w2a8_gemv.
+ *   x_q      device, [M, K] int8 out, or NULL.
+ *   scale    device, [M] float out (per-token absmax), or NULL.
+ *   workspace device, >= bitnet_bitlinear_workspace_bytes(M, N, K) bytes,
+ *            256-byte aligned, any contents.
+ * Shapes the fused kernels do not take (K % 64 != 0, K < 512, unaligned
+ * pointers) run quant_act and the matmul entry points in sequence.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA.
+ */
+int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed, const float *w_scale,
+                     int64_t N, int64_t K, float *y, int8_t *x_q, float *scale, int32_t *acc,
                      void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Bytes of the fixed device array behind bitnet_w2a8_gemv_static_scratch. */

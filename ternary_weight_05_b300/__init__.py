@@ -8,6 +8,7 @@ in the library's CUDA kernels.  Function names follow the C entry points.
     x_q, scale = quant_act(x)                         # x [M, K] bf16/fp32
     y = w2a8_gemv(x_q, scale, packed, beta, N, K)     # decode, M <= 64
     y = w2a8_gemm(x_q, scale, packed, beta, N, K)     # prefill
+    y = bitlinear(x, packed, beta, N, K)              # fused quant + matmul
 """
 from __future__ import annotations
 
@@ -17,7 +18,7 @@ from . import _lib
 from ._lib import BitnetError
 
 __all__ = [
-    "BitnetError", "pack_weights", "quant_act", "w2a8_gemv", "w2a8_gemm", "bitlinear",
+    "BitnetError", "pack_weights", "quant_act", "w2a8_gemv", "w2a8_gemm", "bitlinear", "bitlinear_workspace_bytes",
     "pack_workspace_bytes", "gemv_workspace_bytes", "gemm_workspace_bytes", "check_device_error",
     "set_pdl", "GEMV_MAX_M", "library_path", "w2a8_gemv_static_scratch", "GEMV_STATIC_SCRATCH_BYTES",
 ]
@@ -182,9 +183,39 @@ def w2a8_gemv_static_scratch(x_q, scale, packed, w_scale, N: int, K: int, want_a
     return (y, acc) if want_acc else y
 
 
-def bitlinear(x: torch.Tensor, packed: torch.Tensor, beta: torch.Tensor, N: int, K: int):
-    """quant_act -> GEMV (M <= 64) or GEMM -> fp32 output [M, N]."""
-    x_q, scale = quant_act(x)
-    if x.shape[0] <= GEMV_MAX_M:
-        return w2a8_gemv(x_q, scale, packed, beta, N, K)
-    return w2a8_gemm(x_q, scale, packed, beta, N, K)
+def bitlinear_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_L().bitnet_bitlinear_workspace_bytes(M, N, K))
+
+
+def bitlinear(x: torch.Tensor, packed: torch.Tensor, w_scale: torch.Tensor, N: int, K: int, want_acc: bool = False,
+              want_xq: bool = False, out=None, workspace=None):
+    """Fused BitLinear forward (absmax quantisation inside the matmul kernels).
+
+    x [M, K] bf16/fp32 -> y fp32 [M, N]; with want_acc / want_xq also the exact
+    int32 accumulators and (x_q int8 [M, K], scale fp32 [M]).
+    """
+    for t, nm in ((x, "x"), (packed, "packed"), (w_scale, "w_scale")):
+        _dev(t, nm)
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    M = x.shape[0]
+    dev = x.device
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=dev)
+    acc = torch.empty((M, N), dtype=torch.int32, device=dev) if want_acc else None
+    xq = torch.empty((M, K), dtype=torch.int8, device=dev) if want_xq else None
+    sc = torch.empty(M, dtype=torch.float32, device=dev) if want_xq else None
+    nbytes = bitlinear_workspace_bytes(M, N, K)
+    stream = _stream(dev)
+    if workspace is None:
+        workspace = _ws.get(dev, "bitlinear", nbytes, stream)
+    ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+    st = _L().bitnet_bitlinear(x.data_ptr(), _dtype_code(x), M, packed.data_ptr(), w_scale.data_ptr(), N, K,
+                               y.data_ptr(), ptr(xq), ptr(sc), ptr(acc), workspace.data_ptr(), workspace.numel(),
+                               stream)
+    _lib.check("bitnet_bitlinear", st)
+    res = (y,)
+    if want_acc:
+        res += (acc,)
+    if want_xq:
+        res += (xq, sc)
+    return res[0] if len(res) == 1 else res

@@ -26,6 +26,8 @@ SIGNATURES = {
     "bitnet_w2a8_gemm": (_i, [_p, _p, _i64, _p, _p, _i64, _i64, _p, _p, _p, _sz, _p]),
     "bitnet_check_device_error": (_i, [_p]),
     "bitnet_w2a8_gemv_static_scratch": (_i, [_p, _p, _i64, _p, _p, _i64, _i64, _p, _p, _p]),
+    "bitnet_bitlinear_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "bitnet_bitlinear": (_i, [_p, _i, _i64, _p, _p, _i64, _i64, _p, _p, _p, _p, _p, _sz, _p]),
 }
 
 STATUS = {

@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "gemm.cuh"
 #include "gemv.cuh"
+#include "gemv_tc.cuh"
 #include "gemv_rows.cuh"
 #include "pack.cuh"
 #include "quant_act.cuh"
@@ -105,6 +106,9 @@ bitnet_status set_smem(K kernel, size_t bytes) {
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 constexpr int64_t kMaxElems = (int64_t)1 << 40;
+// The tensor-core paths accumulate code * x (|.| <= 254 per term) in fp32 in
+// units of 2^-24; the sum of a row stays an exact integer while 254 * K < 2^24.
+constexpr int64_t kTensorMaxK = 65536;
 
 bool shape_ok(int64_t N, int64_t K) { return N > 0 && K > 0 && K % 4 == 0 && N <= kMaxElems / K; }
 
@@ -115,7 +119,10 @@ struct GemvPlan {
   int NR, NKB, KBS, S, xrow, grid;
   bool hmma;
   size_t smem;
-  size_t ws_partial_bytes, ws_bytes;
+  // Workspace: [partials | tickets] (must be zero on entry, left zero) at
+  // offset 0 for every kernel, then the tensor-core path's prepared
+  // activations, per-token sums and output scales (any contents).
+  size_t ws_partial_bytes, ws_zero_bytes, ws_prep_xb, ws_prep_sums, ws_bytes;
 };
 
 GemvPlan plan_gemv(int64_t M, int64_t N, int64_t K, int sms) {
@@ -133,13 +140,18 @@ GemvPlan plan_gemv(int64_t M, int64_t N, int64_t K, int sms) {
   pl.grid = (int)std::min<long long>(sms, total);
   pl.smem = gemv_smem_layout((int)M, pl.KBS, pl.xrow).bytes + 1024;
   pl.ws_partial_bytes = (size_t)pl.NR * kStageRows * M * 4;
-  pl.ws_bytes = pl.ws_partial_bytes + (size_t)pl.NR * 4 + 256;
+  pl.ws_zero_bytes = ((pl.ws_partial_bytes + (size_t)pl.NR * 4) + 255) & ~(size_t)255;
+  pl.ws_prep_xb = pl.ws_zero_bytes;
+  pl.ws_prep_sums = pl.ws_prep_xb + gemm_xb_bytes(M, K);
+  pl.ws_bytes = pl.ws_prep_sums + (((size_t)M * 8 + 255) & ~(size_t)255) + 256;
   return pl;
 }
 
 template <class Policy>
 bitnet_status launch_gemv_tma(const CUtensorMap &map, const GemvParams &p, const GemvPlan &pl,
                               cudaStream_t stream) {
+  // the kernel adds split row tiles into zeroed partials and tickets
+  if (cudaMemsetAsync(p.ws_partial, 0, pl.ws_zero_bytes, stream) != cudaSuccess) return BITNET_ERR_CUDA;
   auto k = gemv_tma_kernel<Policy>;
   if (set_smem(k, pl.smem) != BITNET_OK) return BITNET_ERR_CUDA;
   return launch(k, dim3(pl.grid), dim3(kGemvThreads), pl.smem, stream, map, p);
@@ -156,6 +168,124 @@ bitnet_status encode_packed_map(CUtensorMap *map, const uint8_t *packed, int64_t
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? BITNET_OK : BITNET_ERR_CUDA;
+}
+
+// Register-resident rows (one read of x) when the row has at most
+// kQuantThreads * 8 * 8 elements; two passes otherwise.
+template <typename T>
+bitnet_status launch_quant(const T *x, bool vec, int64_t M, int64_t K, int8_t *x_q, float *scale,
+                           cudaStream_t stream) {
+  const dim3 grid((unsigned)M), block(kQuantThreads);
+  const int64_t per = (int64_t)kQuantThreads * 8;
+  if (!vec) return launch(quant_act_kernel<T, false, 0>, grid, block, 0, stream, x, K, x_q, scale);
+  if (K <= per) return launch(quant_act_kernel<T, true, 1>, grid, block, 0, stream, x, K, x_q, scale);
+  if (K <= 2 * per) return launch(quant_act_kernel<T, true, 2>, grid, block, 0, stream, x, K, x_q, scale);
+  if (K <= 4 * per) return launch(quant_act_kernel<T, true, 4>, grid, block, 0, stream, x, K, x_q, scale);
+  if (K <= 8 * per) return launch(quant_act_kernel<T, true, 8>, grid, block, 0, stream, x, K, x_q, scale);
+  return launch(quant_act_kernel<T, true, 0>, grid, block, 0, stream, x, K, x_q, scale);
+}
+
+// Prep grid for the tensor-core GEMV: M token CTAs plus CTAs that zero the
+// split-tile partials and tickets (32 KB each).
+unsigned prep_grid(int64_t M, const GemvPlan &pl) {
+  return (unsigned)(M + std::min<int64_t>(148, cdiv((int64_t)pl.ws_zero_bytes, 32768)));
+}
+
+// The row-range kernel takes one or two tokens whose activation words fit in
+// shared memory beside the weight ring.
+bool rows_ok(int64_t M, int64_t K) { return M <= 2 && M * cdiv(K, kStageK) * kStageK <= kRowsXBudget; }
+
+// Row-range decode GEMV (M <= 2).  XT = int8_t: x_q and scale given;
+// XT = float / bf16: fused form, x quantised in the kernel prologue (x_q and
+// scale then optional outputs).
+template <typename XT>
+bitnet_status launch_gemv_rows(const int8_t *x_q, const float *scale, const void *x, int8_t *xq_out,
+                               float *scale_out, int64_t M, const uint8_t *packed, const float *w_scale, int64_t N,
+                               int64_t K, float *y, int32_t *acc, const DeviceInfo *d, cudaStream_t stream) {
+  GemvRowsParams r = {};
+  r.xq = x_q;
+  r.x = x;
+  r.xq_out = xq_out;
+  r.scale_out = scale_out;
+  r.scale = scale;
+  r.w_scale = w_scale;
+  r.y = y;
+  r.acc = acc;
+  r.N = N;
+  r.K = K;
+  r.M = (int)M;
+  r.NKB = (int)cdiv(K, kStageK);
+  r.units = (int)cdiv(N, 8);
+  r.xrow = r.NKB * kStageK;
+  {
+    // as many 8 KB stages as shared memory holds beside the activations
+    const size_t base = gemv_rows_smem_layout((int)M, r.xrow, 0).bytes + 1024;
+    const size_t per = kRowsStageBytes + 16;
+    const size_t avail = d->smem_optin > base ? d->smem_optin - base : 0;
+    r.NS = (int)std::min<size_t>(kRowsMaxStages, avail / per);
+    if (r.NS < 2) return BITNET_ERR_UNSUPPORTED;
+  }
+  CUtensorMap m64, m8;
+  if (bitnet_status s = encode_packed_map(&m64, packed, N, K, 128, kRowsGroup, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
+  if (bitnet_status s = encode_packed_map(&m8, packed, N, K, 128, 8, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
+  const size_t smem = gemv_rows_smem_layout((int)M, r.xrow, r.NS).bytes + 1024;
+  const int grid = std::min(d->sms, r.units);
+  auto k = M == 1 ? gemv_rows_kernel<1, XT> : gemv_rows_kernel<2, XT>;
+  if (set_smem(k, smem) != BITNET_OK) return BITNET_ERR_CUDA;
+  return launch(k, dim3(grid), dim3(kRowsThreads), smem, stream, m64, m8, r);
+}
+
+// Decode GEMV on the tensor cores (3 <= M <= 64): activation prep, then the
+// stream-K tcgen05 kernel with NT = 16, 32 or 64 token columns.
+// With x_q == nullptr the prepared activations are already in the workspace
+// (the fused BitLinear prologue wrote them).
+bitnet_status launch_gemv_tc(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
+                             const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc, void *workspace,
+                             const GemvPlan &pl, const DeviceInfo *d, cudaStream_t stream) {
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  uint32_t *xb = reinterpret_cast<uint32_t *>(ws + pl.ws_prep_xb);
+  int32_t *xsum = reinterpret_cast<int32_t *>(ws + pl.ws_prep_sums);
+  float *fscale = reinterpret_cast<float *>(ws + pl.ws_prep_sums + (size_t)M * 4);
+  if (x_q) {
+    bitnet_status st = launch(gemm_prep_kernel, dim3(prep_grid(M, pl)), dim3(256), 0, stream, x_q, scale, w_scale,
+                              K, xb, xsum, fscale, M, static_cast<uint4 *>(workspace), (int64_t)(pl.ws_zero_bytes / 16));
+    if (st) return st;
+  }
+  const int NT = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+  CUtensorMap wmap, bmap;
+  if (bitnet_status s = encode_packed_map(&wmap, packed, N, K, 128, kTcRows, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {kTcKB, (cuuint32_t)NT};
+    cuuint32_t estr[2] = {1, 1};
+    if (g_encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xb, dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return BITNET_ERR_CUDA;
+  }
+  GemvTcParams p = {};
+  p.y = y;
+  p.acc = acc;
+  p.xsum = xsum;
+  p.fscale = fscale;
+  p.ws_partial = reinterpret_cast<int32_t *>(ws);
+  p.ws_ticket = reinterpret_cast<unsigned *>(ws + pl.ws_partial_bytes);
+  p.N = N;
+  p.K = K;
+  p.M = (int)M;
+  p.NRT = (int)cdiv(N, kTcRows);
+  p.NCH = (int)cdiv(K, kTcChunkK);
+  p.NKB = (int)(K / kTcKB);
+  p.units = (long long)p.NRT * p.NCH;
+  const int grid = (int)std::min<long long>(d->sms, p.units);
+  auto run = [&](auto kernel, size_t smem) -> bitnet_status {
+    if (set_smem(kernel, smem) != BITNET_OK) return BITNET_ERR_CUDA;
+    return launch(kernel, dim3(grid), dim3(kTcThreads), smem, stream, wmap, bmap, p);
+  };
+  if (NT == 16) return run(gemv_tc_kernel<16>, GemvTcSmem<16>::bytes + 1024);
+  if (NT == 32) return run(gemv_tc_kernel<32>, GemvTcSmem<32>::bytes + 1024);
+  return run(gemv_tc_kernel<64>, GemvTcSmem<64>::bytes + 1024);
 }
 
 bitnet_status check_gemm_args(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
@@ -185,6 +315,9 @@ bitnet_status static_scratch_address(void **out) {
   *out = g_static_scratch_addr[dev];
   return BITNET_OK;
 }
+
+bitnet_status launch_gemm_tc(uint32_t *xb, int32_t *xsum, float *fscale, int64_t M, const uint8_t *packed, int64_t N,
+                             int64_t K, float *y, int32_t *acc, const DeviceInfo *d, cudaStream_t stream);
 
 }  // namespace
 
@@ -270,15 +403,9 @@ int bitnet_quant_act(const void *x, int dtype, int64_t M, int64_t K, int8_t *x_q
   if (bitnet_status s = device_info(&d)) return s;
   const size_t esz = dtype == BITNET_F32 ? 4 : 2;
   const bool vec = aligned(x, 16) && ((K * (int64_t)esz) % 16 == 0) && (K % 8 == 0) && aligned(x_q, 8);
-  const dim3 grid((unsigned)M), block(kQuantThreads);
-  if (dtype == BITNET_F32) {
-    const float *xp = static_cast<const float *>(x);
-    return vec ? launch(quant_act_kernel<float, true>, grid, block, 0, stream, xp, K, x_q, scale)
-               : launch(quant_act_kernel<float, false>, grid, block, 0, stream, xp, K, x_q, scale);
-  }
-  const __nv_bfloat16 *xp = static_cast<const __nv_bfloat16 *>(x);
-  return vec ? launch(quant_act_kernel<__nv_bfloat16, true>, grid, block, 0, stream, xp, K, x_q, scale)
-             : launch(quant_act_kernel<__nv_bfloat16, false>, grid, block, 0, stream, xp, K, x_q, scale);
+  if (dtype == BITNET_F32)
+    return launch_quant(static_cast<const float *>(x), vec, M, K, x_q, scale, stream);
+  return launch_quant(static_cast<const __nv_bfloat16 *>(x), vec, M, K, x_q, scale, stream);
 }
 
 size_t bitnet_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -323,30 +450,11 @@ int bitnet_w2a8_gemv(const int8_t *x_q, const float *scale, int64_t M, const uin
     const int blocks = (int)std::min<long long>(cdiv(items, 8), (long long)d->sms * 16);
     return launch(gemv_generic_kernel, dim3(blocks), dim3(256), 0, stream, p);
   }
-  if (M <= 2 && M * cdiv(K, kStageK) * kStageK <= kRowsXBudget) {
-    // one or two tokens: row-range kernel, whole K per CTA, no workspace use
-    GemvRowsParams r = {};
-    r.xq = x_q;
-    r.scale = scale;
-    r.w_scale = w_scale;
-    r.y = y;
-    r.acc = acc;
-    r.N = N;
-    r.K = K;
-    r.M = (int)M;
-    r.NKB = (int)cdiv(K, kStageK);
-    r.units = (int)cdiv(N, 8);
-    r.xrow = r.NKB * kStageK;
-    CUtensorMap m64, m8;
-    if (bitnet_status s = encode_packed_map(&m64, packed, N, K, 128, kRowsGroup, CU_TENSOR_MAP_SWIZZLE_128B))
-      return s;
-    if (bitnet_status s = encode_packed_map(&m8, packed, N, K, 128, 8, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
-    const size_t smem = gemv_rows_smem_layout((int)M, r.xrow).bytes + 1024;
-    const int grid = std::min(d->sms, r.units);
-    auto k = M == 1 ? gemv_rows_kernel<1> : gemv_rows_kernel<2>;
-    if (set_smem(k, smem) != BITNET_OK) return BITNET_ERR_CUDA;
-    return launch(k, dim3(grid), dim3(kRowsThreads), smem, stream, m64, m8, r);
-  }
+  if (rows_ok(M, K))  // one or two tokens: row-range kernel, whole K per CTA, no workspace use
+    return launch_gemv_rows<int8_t>(x_q, scale, nullptr, nullptr, nullptr, M, packed, w_scale, N, K, y, acc, d,
+                                    stream);
+  if (M >= 3 && K <= kTensorMaxK && aligned(x_q, 16))
+    return launch_gemv_tc(x_q, scale, M, packed, w_scale, N, K, y, acc, workspace, pl, d, stream);
   CUtensorMap map;
   if (bitnet_status s = encode_packed_map(&map, packed, N, K, kStageRowBytes, kStageRows,
                                           CU_TENSOR_MAP_SWIZZLE_128B))
@@ -377,7 +485,7 @@ int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uin
   DeviceInfo *d;
   if (bitnet_status s = device_info(&d)) return s;
 
-  const bool tc_ok = (K % 64 == 0) && K >= 512 && aligned(packed, 16) && aligned(x_q, 16);
+  const bool tc_ok = (K % 64 == 0) && K >= 512 && K <= kTensorMaxK && aligned(packed, 16) && aligned(x_q, 16);
   if (!tc_ok) {
     GemvParams p = {};
     p.packed = packed;
@@ -399,9 +507,18 @@ int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uin
   float *fscale = reinterpret_cast<float *>(ws + gemm_xb_bytes(M, K) + (size_t)M * 4);
 
   bitnet_status st = launch(gemm_prep_kernel, dim3((unsigned)M), dim3(256), 0, stream, x_q, scale, w_scale, K,
-                            xb, xsum, fscale);
+                            xb, xsum, fscale, M, static_cast<uint4 *>(nullptr), (int64_t)0);
   if (st) return st;
+  return launch_gemm_tc(xb, xsum, fscale, M, packed, N, K, y, acc, d, stream);
+}
 
+}  // extern "C"
+
+namespace {
+
+// Main prefill GEMM launch; the prepared activations are at xb (workspace).
+bitnet_status launch_gemm_tc(uint32_t *xb, int32_t *xsum, float *fscale, int64_t M, const uint8_t *packed, int64_t N,
+                             int64_t K, float *y, int32_t *acc, const DeviceInfo *d, cudaStream_t stream) {
   CUtensorMap wmap, bmap;
   if (bitnet_status s = encode_packed_map(&wmap, packed, N, K, 128, kGemmRows, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
   {
@@ -432,6 +549,10 @@ int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uin
   return launch(gemm_tc_kernel, dim3(grid), dim3(kGemmThreads), smem, stream, wmap, bmap, p);
 }
 
+}  // namespace
+
+extern "C" {
+
 // Decode GEMV whose scratch is the file-scope array g_gemv_static_scratch instead of a
 // caller workspace, for callers that cannot allocate device memory.  The
 // array is part of the loaded module: each device that loads the library
@@ -459,6 +580,75 @@ int bitnet_w2a8_gemv_static_scratch(const int8_t *x_q, const float *scale, int64
   // the GEMV needs its scratch zero-filled on entry.
   if (cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) return BITNET_ERR_CUDA;
   return bitnet_w2a8_gemv(x_q, scale, M, packed, w_scale, N, K, y, acc, scratch, need, stream);
+}
+
+size_t bitnet_bitlinear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || !shape_ok(N, K) || M > kMaxElems / K || M > kMaxElems / N) return 0;
+  const size_t base = M <= BITNET_GEMV_MAX_M ? plan_gemv(M, N, K, 148).ws_bytes : gemm_workspace_bytes(M, N, K);
+  // + int8 activations and scales for the unfused fallback
+  return base + (((size_t)M * (size_t)K + 255) & ~(size_t)255) + (((size_t)M * 4 + 255) & ~(size_t)255);
+}
+
+int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed, const float *w_scale, int64_t N,
+                     int64_t K, float *y, int8_t *x_q, float *scale, int32_t *acc, void *workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
+  if (!x || !packed || !w_scale || !y) return BITNET_ERR_INVALID_ARG;
+  if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_ERR_INVALID_ARG;
+  if (M <= 0 || !shape_ok(N, K) || M > kMaxElems / K || M > kMaxElems / N) return BITNET_ERR_SHAPE;
+  if (N > 0x7fffffff || K > 0x7fffffff || M > 0x7fffffff) return BITNET_ERR_SHAPE;
+  const size_t esz = dtype == BITNET_F32 ? 4 : 2;
+  if (!aligned(x, esz) || !aligned(w_scale, 4) || !aligned(y, 4) || !aligned(scale, 4) || !aligned(acc, 4))
+    return BITNET_ERR_ALIGNMENT;
+  const size_t need = bitnet_bitlinear_workspace_bytes(M, N, K);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return BITNET_ERR_WORKSPACE;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
+
+  const bool fused = aligned(x, 16) && (K % 64 == 0) && K >= kStageK && aligned(packed, 16) && aligned(x_q, 16);
+  const bool bf = dtype == BITNET_BF16;
+  if (fused && rows_ok(M, K)) {
+    return bf ? launch_gemv_rows<__nv_bfloat16>(nullptr, nullptr, x, x_q, scale, M, packed, w_scale, N, K, y, acc, d,
+                                                stream)
+              : launch_gemv_rows<float>(nullptr, nullptr, x, x_q, scale, M, packed, w_scale, N, K, y, acc, d, stream);
+  }
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  if (fused && K <= kTensorMaxK) {
+    uint32_t *xb;
+    int32_t *xsum;
+    float *fscale;
+    GemvPlan pl = {};
+    if (M <= BITNET_GEMV_MAX_M) {
+      pl = plan_gemv(M, N, K, d->sms);
+      xb = reinterpret_cast<uint32_t *>(ws + pl.ws_prep_xb);
+      xsum = reinterpret_cast<int32_t *>(ws + pl.ws_prep_sums);
+    } else {
+      xb = reinterpret_cast<uint32_t *>(ws);
+      xsum = reinterpret_cast<int32_t *>(ws + gemm_xb_bytes(M, K));
+    }
+    fscale = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(xsum) + (size_t)M * 4);
+    const bool gemv = M <= BITNET_GEMV_MAX_M;
+    const dim3 pgrid = gemv ? dim3(prep_grid(M, pl)) : dim3((unsigned)M);
+    uint4 *zero = gemv ? static_cast<uint4 *>(workspace) : nullptr;
+    const int64_t zero_n16 = gemv ? (int64_t)(pl.ws_zero_bytes / 16) : 0;
+    bitnet_status st =
+        bf ? launch(fused_prep_kernel<__nv_bfloat16>, pgrid, dim3(256), 0, stream,
+                    static_cast<const __nv_bfloat16 *>(x), w_scale, K, xb, xsum, fscale, x_q, scale, M, zero, zero_n16)
+           : launch(fused_prep_kernel<float>, pgrid, dim3(256), 0, stream, static_cast<const float *>(x), w_scale, K,
+                    xb, xsum, fscale, x_q, scale, M, zero, zero_n16);
+    if (st) return st;
+    if (M <= BITNET_GEMV_MAX_M)
+      return launch_gemv_tc(nullptr, nullptr, M, packed, w_scale, N, K, y, acc, workspace, pl, d, stream);
+    return launch_gemm_tc(xb, xsum, fscale, M, packed, N, K, y, acc, d, stream);
+  }
+  // Unfused: quantise into the caller's buffers or the workspace tail, then
+  // the GEMV / GEMM entry points.
+  const size_t base = M <= BITNET_GEMV_MAX_M ? plan_gemv(M, N, K, d->sms).ws_bytes : gemm_workspace_bytes(M, N, K);
+  int8_t *xq_buf = x_q ? x_q : reinterpret_cast<int8_t *>(ws + base);
+  float *s_buf = scale ? scale : reinterpret_cast<float *>(ws + base + (((size_t)M * (size_t)K + 255) & ~(size_t)255));
+  if (int st = bitnet_quant_act(x, dtype, M, K, xq_buf, s_buf, stream)) return st;
+  if (M <= BITNET_GEMV_MAX_M)
+    return bitnet_w2a8_gemv(xq_buf, s_buf, M, packed, w_scale, N, K, y, acc, workspace, base, stream);
+  return bitnet_w2a8_gemm(xq_buf, s_buf, M, packed, w_scale, N, K, y, acc, workspace, base, stream);
 }
 
 int bitnet_check_device_error(cudaStream_t stream) {

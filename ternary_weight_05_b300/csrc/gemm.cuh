@@ -20,21 +20,32 @@
 //     D * 2^24 - sum_k x_q is the exact integer accumulator.
 //   * Two accumulators (256 TMEM columns) let the epilogue of one tile overlap
 //     the MMAs of the next.
-// Warp roles: 0 TMA producer, 1 TMEM owner + MMA issuer, 4-7 decoders,
-// 8-11 epilogue.  Every wait is bounded (kWaitLimitNs); on expiry the CTA
+// Warp roles: 0 TMA producer, 1 TMEM owner + MMA issuer, 4-7 decoders (set
+// 0), 8-11 epilogue, 12-15 ... further decoder sets.  Decoder set d takes
+// the K-blocks c with c % kGemmDecSets == d, so several blocks are in
+// flight per TMEM lane quarter while each warp waits for its tcgen05.st.  Every wait is bounded (kWaitLimitNs); on expiry the CTA
 // records the error, stops issuing work, drains what it issued, frees TMEM
 // and exits.
 #pragma once
 
 #include "common.cuh"
+#include "quant_act.cuh"
 
 namespace bitnet {
 
-constexpr int kGemmThreads = 384;
+#ifndef BITNET_GEMM_DEC_SETS
+#define BITNET_GEMM_DEC_SETS 2
+#endif
+#ifndef BITNET_GEMM_STAGES
+#define BITNET_GEMM_STAGES 8
+#endif
+constexpr int kGemmDecSets = BITNET_GEMM_DEC_SETS;  // decoder warp sets of 4 warps
+constexpr int kGemmThreads = 384 + (kGemmDecSets - 1) * 128;
 constexpr int kGemmRows = 128;   // weight rows per tile (MMA M)
 constexpr int kGemmTok = 128;    // tokens per tile (MMA N)
 constexpr int kGemmKB = 64;      // K per pipeline step (4 MMAs of K = 16)
-constexpr int kGemmStages = 6;   // B stages in smem == A buffers in TMEM
+constexpr int kGemmStages = BITNET_GEMM_STAGES;  // B stages in smem == A buffers in TMEM (<= 8)
+static_assert(kGemmStages <= 8, "A buffers must fit beside the accumulators in TMEM");
 constexpr int kGemmBStageBytes = kGemmTok * 128;
 constexpr int kGemmWStages = 2;  // packed-weight stages (128 rows x 512 K)
 constexpr int kGemmWStageBytes = kGemmRows * 128;
@@ -56,12 +67,15 @@ struct GemmSmem {
   int bstage, wstage, bars, tmem_slot, flags, bytes;
 };
 
+// Barriers: 3 per B stage, 2 per weight stage, 4 accumulator, 1 drain.
+constexpr int kGemmBarBytes = ((3 * kGemmStages + 2 * kGemmWStages + 5) * 8 + 15) / 16 * 16;
+
 __host__ __device__ constexpr GemmSmem gemm_smem_layout() {
   return GemmSmem{0, kGemmStages * kGemmBStageBytes,
                   kGemmStages * kGemmBStageBytes + kGemmWStages * kGemmWStageBytes,
-                  kGemmStages * kGemmBStageBytes + kGemmWStages * kGemmWStageBytes + 256,
-                  kGemmStages * kGemmBStageBytes + kGemmWStages * kGemmWStageBytes + 272,
-                  kGemmStages * kGemmBStageBytes + kGemmWStages * kGemmWStageBytes + 288};
+                  kGemmStages * kGemmBStageBytes + kGemmWStages * kGemmWStageBytes + kGemmBarBytes,
+                  kGemmStages * kGemmBStageBytes + kGemmWStages * kGemmWStageBytes + kGemmBarBytes + 16,
+                  kGemmStages * kGemmBStageBytes + kGemmWStages * kGemmWStageBytes + kGemmBarBytes + 32};
 }
 
 // ---------------------------------------------------------- tcgen05 PTX --
@@ -120,6 +134,17 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart (rows of 128 bytes), descriptor version 1.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
@@ -134,15 +159,49 @@ __host__ __device__ constexpr uint32_t gemm_idesc(int m, int n) {
 
 // --------------------------------------------------------------- prep --
 
+// One 16-K group of int8 activations in the B layout: element 2i+h of the
+// group is x[8h + i] * 4^-e(i), e = {0,1,2,3,4,5,0,1}, as fp16 (exact: at most
+// 7 significant bits, no smaller than 2^-10).  Returns the sum of the group.
+__device__ __forceinline__ int prep_group(const int8_t (&v)[16], uint32_t *out) {
+  uint32_t h[8];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = i < 6 ? i : i - 6;
+    const float sc = 1.0f / (float)(1 << (2 * e));
+    h[i] = (uint32_t)__half_as_ushort(__float2half_rn((float)v[i] * sc)) |
+           ((uint32_t)__half_as_ushort(__float2half_rn((float)v[8 + i] * sc)) << 16);
+    sum += v[i] + v[8 + i];
+  }
+  uint4 *dst = reinterpret_cast<uint4 *>(out);
+  dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+  dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  return sum;
+}
+
+// CTAs past the M token rows of a prep kernel zero `zero` (n16 16-byte
+// words: the split-tile partial sums and tickets of the GEMV that follows),
+// after the previous kernel, which may share the workspace, has finished.
+__device__ __forceinline__ void prep_zero_tail(int64_t M, uint4 *zero, int64_t n16) {
+  const int64_t cta = (int64_t)blockIdx.x - M, nct = (int64_t)gridDim.x - M;
+  for (int64_t i = cta * 256 + threadIdx.x; i < n16; i += nct * 256) zero[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // x_q int8 [M, K] -> fp16 B matrix [M, K] (per 16-K group, element 2i+h is
 // x[16q + 8h + i] * 4^-e(i), e = {0,1,2,3,4,5,0,1}), per-token sum of x_q and
-// the per-token output scale w_scale * s_m / 127.  One CTA per token.
+// the per-token output scale w_scale * s_m / 127.  One CTA per token (CTAs
+// beyond M zero the GEMV's partial sums).
 __global__ void __launch_bounds__(256) gemm_prep_kernel(const int8_t *__restrict__ xq, const float *__restrict__ scale,
                                                         const float *__restrict__ w_scale, int64_t K,
                                                         uint32_t *__restrict__ xb, int32_t *__restrict__ xsum,
-                                                        float *__restrict__ fscale) {
-  pdl_wait_prior_grid();
+                                                        float *__restrict__ fscale, int64_t M, uint4 *zero,
+                                                        int64_t zero_n16) {
   pdl_launch_dependents();
+  pdl_wait_prior_grid();
+  if ((int64_t)blockIdx.x >= M) {
+    prep_zero_tail(M, zero, zero_n16);
+    return;
+  }
   __shared__ int red[8];
   const int64_t m = blockIdx.x;
   const int8_t *row = xq + m * K;
@@ -152,18 +211,7 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const int8_t *__restrict
     const int4 u = *reinterpret_cast<const int4 *>(row + q * 16);
     int8_t v[16];
     memcpy(v, &u, 16);
-    uint32_t h[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = i < 6 ? i : i - 6;
-      const float sc = 1.0f / (float)(1 << (2 * e));
-      h[i] = (uint32_t)__half_as_ushort(__float2half_rn((float)v[i] * sc)) |
-             ((uint32_t)__half_as_ushort(__float2half_rn((float)v[8 + i] * sc)) << 16);
-      sum += v[i] + v[8 + i];
-    }
-    uint4 *dst = reinterpret_cast<uint4 *>(out + q * 8);
-    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    sum += prep_group(v, out + q * 8);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -177,6 +225,68 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const int8_t *__restrict
   }
 }
 
+// Fused BitLinear prologue for the tensor-core paths: per-token absmax
+// quantisation of x (BitNet 深度拆解 §2.2, the same fp32 operations as
+// quant_act_kernel) straight into the B layout, the per-token sum of x_q and
+// the output scale.  Optionally also writes x_q and s.  One CTA per token;
+// K % 16 == 0 and 16-byte aligned rows (checked on the host).
+template <typename T>
+__global__ void __launch_bounds__(256)
+    fused_prep_kernel(const T *__restrict__ x, const float *__restrict__ w_scale, int64_t K,
+                      uint32_t *__restrict__ xb, int32_t *__restrict__ xsum, float *__restrict__ fscale,
+                      int8_t *__restrict__ xq_out, float *__restrict__ scale_out, int64_t M, uint4 *zero,
+                      int64_t zero_n16) {
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
+  if ((int64_t)blockIdx.x >= M) {
+    prep_zero_tail(M, zero, zero_n16);
+    return;
+  }
+  __shared__ float redf[8];
+  __shared__ int red[8];
+  const int64_t m = blockIdx.x;
+  const T *row = x + m * K;
+  uint32_t *out = xb + m * (K / 2);
+  float amax = 0.0f;
+  for (int64_t k = (int64_t)threadIdx.x * 8; k < K; k += 256 * 8) {
+    float v[8];
+    load8(row + k, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+  amax = block_max_256(amax, redf);
+  const float s = amax < 1e-8f ? 1e-8f : amax;
+  int sum = 0;
+  for (int64_t q = threadIdx.x; q < K / 16; q += 256) {
+    float f[8], g[8];
+    load8(row + q * 16, f);
+    load8(row + q * 16 + 8, g);
+    int8_t v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] = quantize_one(f[i], s);
+      v[8 + i] = quantize_one(g[i], s);
+    }
+    if (xq_out) {
+      int4 u;
+      memcpy(&u, v, 16);
+      *reinterpret_cast<int4 *>(xq_out + m * K + q * 16) = u;
+    }
+    sum += prep_group(v, out + q * 8);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int w = 0; w < 8; ++w) t += red[w];
+    xsum[m] = t;
+    fscale[m] = __fdiv_rn(__fmul_rn(__ldg(w_scale), s), 127.0f);
+    if (scale_out) scale_out[m] = s;
+  }
+}
+
 // --------------------------------------------------------------- main --
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -185,9 +295,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr GemmSmem L = gemm_smem_layout();
-  uint64_t *bfull = reinterpret_cast<uint64_t *>(smem + L.bars);  // [6] TMA -> MMA
-  uint64_t *kempty = bfull + kGemmStages;                            // [6] MMA done -> producer, decoders
-  uint64_t *afull = kempty + kGemmStages;                            // [6] decoders -> MMA
+  uint64_t *bfull = reinterpret_cast<uint64_t *>(smem + L.bars);  // [stages] TMA -> MMA
+  uint64_t *kempty = bfull + kGemmStages;                            // [stages] MMA done -> producer, decoders
+  uint64_t *afull = kempty + kGemmStages;                            // [stages] decoders -> MMA
   uint64_t *wfull = afull + kGemmStages;                             // [2] TMA -> decoders
   uint64_t *wempty = wfull + kGemmWStages;                           // [2] decoders -> producer
   uint64_t *accfull = wempty + kGemmWStages;                         // [2] MMA -> epilogue
@@ -197,6 +307,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flags);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kGemmStages; ++i) {
@@ -206,7 +317,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int i = 0; i < kGemmWStages; ++i) {
       mbar_init(&wfull[i], 1);
-      mbar_init(&wempty[i], 4);
+      mbar_init(&wempty[i], 4 * kGemmDecSets);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accfull[i], 1);
@@ -304,10 +415,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_commit(drain);
       mbar_wait(drain, 0);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if ((warp >= 4 && warp < 8) || warp >= 12) {
     // ---------------------------------------------------------- decoders --
     // tcgen05.st is warp-collective: the abort decision is made warp-uniform.
     pdl_wait_prior_grid();
+    const int dset = warp < 8 ? 0 : 1 + (warp - 12) / 4;
     const int quad = warp & 3, row = quad * 32 + lane;
     const uint32_t wbase = smem_u32(smem + L.wstage);
     long long c = 0, wc = 0;
@@ -316,6 +428,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int kb = 0; kb < p.NKB; ++kb, ++c) {
         const int ws = (int)(wc % kGemmWStages);
         if ((kb & 7) == 0) wait(&wfull[ws], (uint32_t)((wc / kGemmWStages) & 1));
+        const int chunk = kb & 7;
+        const bool last_of_wstage = chunk == 7 || kb == p.NKB - 1;
+        if ((int)(c % kGemmDecSets) != dset) {  // another set decodes this block
+          if (__any_sync(0xffffffffu, *abort_flag)) {
+            stop = true;
+            break;
+          }
+          if (last_of_wstage) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wempty[ws]);
+            ++wc;
+          }
+          continue;
+        }
         const int s = (int)(c % kGemmStages);
         if (c >= kGemmStages) wait(&kempty[s], (uint32_t)(((c / kGemmStages) - 1) & 1));
         if (__any_sync(0xffffffffu, *abort_flag)) {
@@ -323,7 +449,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         tc_fence_after();
-        const int chunk = kb & 7;
         const uint4 v = lds_u128(wbase + ws * kGemmWStageBytes + row * 128 + (((chunk ^ (row & 7)) & 7) << 4));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t h[32];
@@ -339,13 +464,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&afull[s]);
-        if (chunk == 7 || kb == p.NKB - 1) {
+        if (last_of_wstage) {
           if (lane == 0) mbar_arrive(&wempty[ws]);
           ++wc;
         }
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 8 && warp < 12) {
     // ---------------------------------------------------------- epilogue --
     pdl_wait_prior_grid();
     const int quad = warp & 3, row = quad * 32 + lane;

@@ -438,6 +438,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   const long long g1 = p.total * (blockIdx.x + 1) / gridDim.x;
   const int count = (int)(g1 - g0);
   const int tid = threadIdx.x, lane = tid & 31;
+  pdl_launch_dependents();
 
   if (tid == 0) {
     for (int i = 0; i < kGemvStages; ++i) {
@@ -469,7 +470,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     for (; issued < count && issued < kGemvStages; ++issued) issue(issued);
   }
   pdl_wait_prior_grid();
-  pdl_launch_dependents();
   if (tid < p.M) fscale[tid] = __fdiv_rn(__fmul_rn(__ldg(p.w_scale), __ldg(p.scale + tid)), 127.0f);
 
   Policy pol;
@@ -526,6 +526,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 // multiple of 64, K < 512, unaligned packed rows).  One warp per (row, token);
 // lanes stride over the row's bytes.
 __global__ void gemv_generic_kernel(const GemvParams p) {
+  pdl_launch_dependents();
   pdl_wait_prior_grid();
   const uint8_t *packed = p.packed;
   const int lane = threadIdx.x & 31;

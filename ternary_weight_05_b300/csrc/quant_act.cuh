@@ -5,7 +5,10 @@
 // with round-half-even.  Every operation is the single IEEE fp32 operation
 // the formula names (division first, then the multiply by 127).
 //
-// One CTA per token row; two passes over the row (the second hits L1/L2).
+// One CTA per token row.  When the row fits in registers (R vectors of 8
+// elements per thread) it is read from memory once: absmax, block reduction,
+// then quantisation from the registers.  Longer rows take two passes (the
+// second hits L1/L2).
 #pragma once
 
 #include "common.cuh"
@@ -51,20 +54,59 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
   }
 }
 
+// Packs the int8 codes of 8 elements into two words.
+__device__ __forceinline__ uint2 quantize8(const float (&v)[8], float s) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) lo |= (uint32_t)(uint8_t)quantize_one(v[i], s) << (8 * i);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) hi |= (uint32_t)(uint8_t)quantize_one(v[4 + i], s) << (8 * i);
+  return make_uint2(lo, hi);
+}
+
 // VEC: the row start of x is 16-byte aligned, K is a multiple of 8 and the
 // x_q row start is 8-byte aligned, so 8 elements move per access.
-template <typename T, bool VEC>
+// R > 0 (VEC only): K <= kQuantThreads * 8 * R, the row is held in registers.
+template <typename T, bool VEC, int R>
 __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const T *__restrict__ x, int64_t K,
                                                                   int8_t *__restrict__ xq,
                                                                   float *__restrict__ scale) {
   __shared__ float red[kQuantThreads / 32];
-  pdl_wait_prior_grid();
+  // Let the next kernel launch (and prefetch its weights) right away; it
+  // still waits for this grid to complete before reading x_q.
   pdl_launch_dependents();
+  pdl_wait_prior_grid();
   const int64_t m = blockIdx.x;
   const T *row = x + m * K;
   int8_t *qrow = xq + m * K;
 
   float amax = 0.0f;
+  if (VEC && R > 0) {
+    float v[R > 0 ? R : 1][8];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int64_t k = ((int64_t)threadIdx.x + (int64_t)r * kQuantThreads) * 8;
+      if (k < K) {
+        load8(row + k, v[r]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[r][i] = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[r][i]));
+    amax = block_max_256(amax, red);
+    const float s = amax < 1e-8f ? 1e-8f : amax;
+    if (threadIdx.x == 0) scale[m] = s;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int64_t k = ((int64_t)threadIdx.x + (int64_t)r * kQuantThreads) * 8;
+      if (k < K) *reinterpret_cast<uint2 *>(qrow + k) = quantize8(v[r], s);
+    }
+    return;
+  }
   if (VEC) {
     for (int64_t k = (int64_t)threadIdx.x * 8; k < K; k += kQuantThreads * 8) {
       float v[8];
@@ -83,12 +125,7 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const T *__res
     for (int64_t k = (int64_t)threadIdx.x * 8; k < K; k += kQuantThreads * 8) {
       float v[8];
       load8(row + k, v);
-      uint32_t lo = 0, hi = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) lo |= (uint32_t)(uint8_t)quantize_one(v[i], s) << (8 * i);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) hi |= (uint32_t)(uint8_t)quantize_one(v[4 + i], s) << (8 * i);
-      *reinterpret_cast<uint2 *>(qrow + k) = make_uint2(lo, hi);
+      *reinterpret_cast<uint2 *>(qrow + k) = quantize8(v, s);
     }
   } else {
     for (int64_t k = threadIdx.x; k < K; k += kQuantThreads) qrow[k] = quantize_one(load_as_f32(row, k), s);

@@ -31,7 +31,11 @@ def assert_y_close(y, y_ref):
 # ------------------------------------------------------------- quant_act ---
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("M,K", [(1, 1), (1, 7), (3, 100), (2, 2560), (5, 6912), (17, 8192), (64, 1000)])
+# K spans every kernel variant: scalar (K % 8 != 0), rows held in registers
+# with 1, 2, 4 or 8 vectors per thread (K <= 2048, 4096, 8192, 16384), and
+# the two-pass loop for longer rows.
+@pytest.mark.parametrize("M,K", [(1, 1), (1, 7), (3, 100), (2, 2560), (5, 6912), (17, 8192), (64, 1000), (1, 2048),
+                                 (1, 2056), (2, 12288), (1, 16384), (3, 20000), (1, 28672)])
 def test_quant_act_random(lib, oracle_mod, cuda_dev, dtype, M, K):
     import torch
 
@@ -149,6 +153,53 @@ def test_gemv_tma_path(lib, oracle_mod, cuda_dev, M, N, K):
 @pytest.mark.parametrize("M,N,K", [(1, 7, 4), (3, 5, 12), (2, 33, 100), (5, 64, 448), (64, 9, 1000)])
 def test_gemv_generic_path(lib, oracle_mod, cuda_dev, M, N, K):
     gemv_case(lib, oracle_mod, cuda_dev, M, N, K, seed=M + N + K)
+
+
+@pytest.mark.parametrize("fn", ["gemv", "gemm"])
+@pytest.mark.parametrize("M", [1, 3, 20])
+def test_matmul_beyond_fp32_exact_k(lib, oracle_mod, cuda_dev, fn, M):
+    # K = 66048: every weight +1, every activation 127, so sum code * x reaches
+    # 2 * 127 * K > 2^24, past what fp32 tensor-core accumulation holds
+    # exactly; such shapes must take an exact path.
+    import torch
+
+    N, K = 40, 66048
+    q = np.ones((N, K), dtype=np.int8)
+    q[1::2, ::3] = -1
+    packed = oracle_mod.pack_codes(q)
+    xq = np.full((M, K), 127, dtype=np.int8)
+    xq[-1, ::5] = -127
+    s = np.full(M, 3.0, dtype=np.float32)
+    acc_ref = oracle_mod.contract(xq, packed, N, K, threads=8)
+    y_ref = oracle_mod.epilogue(acc_ref, s, 0.5)
+    f = lib.w2a8_gemv if fn == "gemv" else lib.w2a8_gemm
+    y, acc = f(to_dev(xq, cuda_dev), to_dev(s, cuda_dev), to_dev(packed, cuda_dev),
+               to_dev(np.array([0.5], np.float32), cuda_dev), N, K, want_acc=True)
+    assert np.array_equal(acc.cpu().numpy(), acc_ref)
+    assert_y_close(y.cpu().numpy(), y_ref)
+
+
+def test_gemv_workspace_any_contents(lib, oracle_mod, cuda_dev):
+    # one workspace, filled with garbage, shared by calls of different shapes
+    # and paths (tensor-core stream-K, row-range, mma.sync stream-K for
+    # K > 65536): each call zeroes what it accumulates into
+    import torch
+
+    cases = [(64, 1, 512), (3, 129, 1024), (16, 300, 2560), (1, 257, 2624), (40, 2000, 1024), (5, 24, 66048),
+             (3, 129, 1024)]
+    nbytes = max(lib.gemv_workspace_bytes(M, N, K) for M, N, K in cases)
+    ws = torch.full((nbytes,), 0xAB, dtype=torch.uint8, device=cuda_dev)
+    for i, (M, N, K) in enumerate(cases):
+        rng = np.random.default_rng(i)
+        q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+        packed = oracle_mod.pack_codes(q)
+        xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+        s = (rng.random(M) + 0.5).astype(np.float32)
+        acc_ref = oracle_mod.contract(xq, packed, N, K, threads=8)
+        y, acc = lib.w2a8_gemv(to_dev(xq, cuda_dev), to_dev(s, cuda_dev), to_dev(packed, cuda_dev),
+                               to_dev(np.array([0.75], np.float32), cuda_dev), N, K, want_acc=True, workspace=ws)
+        assert np.array_equal(acc.cpu().numpy(), acc_ref), (M, N, K)
+        assert_y_close(y.cpu().numpy(), oracle_mod.epilogue(acc_ref, s, 0.75))
 
 
 def test_gemv_unaligned_packed_pointer(lib, oracle_mod, cuda_dev):
