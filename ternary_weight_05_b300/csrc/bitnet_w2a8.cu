@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "gemm.cuh"
 #include "gemv.cuh"
+#include "gemv_ldg.cuh"
 #include "gemv_tc.cuh"
 #include "gemv_rows.cuh"
 #include "pack.cuh"
@@ -189,6 +190,50 @@ bitnet_status launch_quant(const T *x, bool vec, int64_t M, int64_t K, int8_t *x
 // split-tile partials and tickets (32 KB each).
 unsigned prep_grid(int64_t M, const GemvPlan &pl) {
   return (unsigned)(M + std::min<int64_t>(148, cdiv((int64_t)pl.ws_zero_bytes, 32768)));
+}
+
+// The streaming-load kernel takes one or two tokens whose activation words
+// fit in registers: 16-byte chunks per row <= 32 lanes x 4 (one token) or x 2.
+int ldg_chunks_per_lane(int64_t M, int64_t K) { return (int)cdiv(K / 64, 32) * (M == 1 ? 1 : 2); }
+bool ldg_ok(int64_t M, int64_t K, const void *packed) {
+  return M <= 2 && K % 64 == 0 && aligned(packed, 16) && ldg_chunks_per_lane(M, K) <= 4;
+}
+
+template <typename XT>
+bitnet_status launch_gemv_ldg(const int8_t *x_q, const float *scale, const void *x, int8_t *xq_out, float *scale_out,
+                              int64_t M, const uint8_t *packed, const float *w_scale, int64_t N, int64_t K, float *y,
+                              int32_t *acc, const DeviceInfo *d, cudaStream_t stream) {
+  GemvLdgParams p = {};
+  p.packed = packed;
+  p.xq = x_q;
+  p.x = x;
+  p.xq_out = xq_out;
+  p.scale_out = scale_out;
+  p.scale = scale;
+  p.w_scale = w_scale;
+  p.y = y;
+  p.acc = acc;
+  p.N = N;
+  p.K = K;
+  p.M = (int)M;
+  p.C = (int)(K / 64);
+  p.SR = (int)std::max<int64_t>(1, kLdgStageBytes / (K / 4));
+  const int J = (int)cdiv(p.C, 32);
+  const size_t smem = gemv_ldg_smem_layout((int)M, p.C).bytes + 128;
+  const int grid = (int)std::min<int64_t>(d->sms, cdiv(N, kLdgWarps));
+  auto run = [&](auto kernel) -> bitnet_status {
+    if (set_smem(kernel, smem) != BITNET_OK) return BITNET_ERR_CUDA;
+    return launch(kernel, dim3(grid), dim3(kLdgThreads), smem, stream, p);
+  };
+  if (M == 1) {
+    switch (J) {
+      case 1: return run(gemv_ldg_kernel<1, 1, XT>);
+      case 2: return run(gemv_ldg_kernel<1, 2, XT>);
+      case 3: return run(gemv_ldg_kernel<1, 3, XT>);
+      default: return run(gemv_ldg_kernel<1, 4, XT>);
+    }
+  }
+  return J == 1 ? run(gemv_ldg_kernel<2, 1, XT>) : run(gemv_ldg_kernel<2, 2, XT>);
 }
 
 // The row-range kernel takes one or two tokens whose activation words fit in
@@ -450,6 +495,8 @@ int bitnet_w2a8_gemv(const int8_t *x_q, const float *scale, int64_t M, const uin
     const int blocks = (int)std::min<long long>(cdiv(items, 8), (long long)d->sms * 16);
     return launch(gemv_generic_kernel, dim3(blocks), dim3(256), 0, stream, p);
   }
+  if (ldg_ok(M, K, packed) && aligned(x_q, 16))  // one or two tokens, rows up to 8192 / 4096
+    return launch_gemv_ldg<int8_t>(x_q, scale, nullptr, nullptr, nullptr, M, packed, w_scale, N, K, y, acc, d, stream);
   if (rows_ok(M, K))  // one or two tokens: row-range kernel, whole K per CTA, no workspace use
     return launch_gemv_rows<int8_t>(x_q, scale, nullptr, nullptr, nullptr, M, packed, w_scale, N, K, y, acc, d,
                                     stream);
@@ -606,6 +653,11 @@ int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed,
 
   const bool fused = aligned(x, 16) && (K % 64 == 0) && K >= kStageK && aligned(packed, 16) && aligned(x_q, 16);
   const bool bf = dtype == BITNET_BF16;
+  if (fused && ldg_ok(M, K, packed)) {
+    return bf ? launch_gemv_ldg<__nv_bfloat16>(nullptr, nullptr, x, x_q, scale, M, packed, w_scale, N, K, y, acc, d,
+                                               stream)
+              : launch_gemv_ldg<float>(nullptr, nullptr, x, x_q, scale, M, packed, w_scale, N, K, y, acc, d, stream);
+  }
   if (fused && rows_ok(M, K)) {
     return bf ? launch_gemv_rows<__nv_bfloat16>(nullptr, nullptr, x, x_q, scale, M, packed, w_scale, N, K, y, acc, d,
                                                 stream)
