@@ -16,6 +16,7 @@
 #include "gemv.cuh"
 #include "gemv_ldg.cuh"
 #include "gemv_tc.cuh"
+#include "gemv_mma.cuh"
 #include "gemv_rows.cuh"
 #include "pack.cuh"
 #include "quant_act.cuh"
@@ -296,7 +297,9 @@ bitnet_status launch_gemv_tc(const int8_t *x_q, const float *scale, int64_t M, c
                               K, xb, xsum, fscale, M, static_cast<uint4 *>(workspace), (int64_t)(pl.ws_zero_bytes / 16));
     if (st) return st;
   }
-  const int NT = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+  // 3..16 tokens: mma.sync kernel (8 or 16 token rows); 17..64: tcgen05 kernel
+  const bool mma = M <= 16;
+  const int NT = mma ? (M <= 8 ? 8 : 16) : (M <= 32 ? 32 : 64);
   CUtensorMap wmap, bmap;
   if (bitnet_status s = encode_packed_map(&wmap, packed, N, K, 128, kTcRows, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
   {
@@ -323,7 +326,16 @@ bitnet_status launch_gemv_tc(const int8_t *x_q, const float *scale, int64_t M, c
   p.NCH = (int)cdiv(K, kTcChunkK);
   p.NKB = (int)(K / kTcKB);
   p.units = (long long)p.NRT * p.NCH;
-  const int grid = (int)std::min<long long>(d->sms, p.units);
+  if (mma) {
+    const int grid = (int)std::min<long long>(d->sms, p.units);
+    auto runm = [&](auto kernel, size_t smem) -> bitnet_status {
+      if (set_smem(kernel, smem) != BITNET_OK) return BITNET_ERR_CUDA;
+      return launch(kernel, dim3(grid), dim3(kMmaThreads), smem, stream, wmap, bmap, p);
+    };
+    return NT == 8 ? runm(gemv_mma_kernel<1>, GemvMmaSmem<1>::bytes + 1024)
+                   : runm(gemv_mma_kernel<2>, GemvMmaSmem<2>::bytes + 1024);
+  }
+  const int grid = (int)std::min<long long>((long long)d->sms * kTcCtasPerSm, p.units);
   auto run = [&](auto kernel, size_t smem) -> bitnet_status {
     if (set_smem(kernel, smem) != BITNET_OK) return BITNET_ERR_CUDA;
     return launch(kernel, dim3(grid), dim3(kTcThreads), smem, stream, wmap, bmap, p);

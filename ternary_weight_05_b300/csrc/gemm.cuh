@@ -37,12 +37,18 @@ namespace bitnet {
 #define BITNET_GEMM_DEC_SETS 2
 #endif
 #ifndef BITNET_GEMM_STAGES
-#define BITNET_GEMM_STAGES 8
+#define BITNET_GEMM_STAGES 4
 #endif
 constexpr int kGemmDecSets = BITNET_GEMM_DEC_SETS;  // decoder warp sets of 4 warps
 constexpr int kGemmThreads = 384 + (kGemmDecSets - 1) * 128;
 constexpr int kGemmRows = 128;   // weight rows per tile (MMA M)
-constexpr int kGemmTok = 128;    // tokens per tile (MMA N)
+#ifndef BITNET_GEMM_TOK
+#define BITNET_GEMM_TOK 256
+#endif
+constexpr int kGemmTok = BITNET_GEMM_TOK;  // tokens per tile (MMA N): 128 or 256
+// Accumulator buffers in TMEM: two (the epilogue of one tile overlaps the
+// MMAs of the next) when they fit beside the A buffers, else one.
+constexpr int kGemmAccBufs = kGemmTok <= 128 ? 2 : 1;
 constexpr int kGemmKB = 64;      // K per pipeline step (4 MMAs of K = 16)
 constexpr int kGemmStages = BITNET_GEMM_STAGES;  // B stages in smem == A buffers in TMEM (<= 8)
 static_assert(kGemmStages <= 8, "A buffers must fit beside the accumulators in TMEM");
@@ -50,8 +56,8 @@ constexpr int kGemmBStageBytes = kGemmTok * 128;
 constexpr int kGemmWStages = 2;  // packed-weight stages (128 rows x 512 K)
 constexpr int kGemmWStageBytes = kGemmRows * 128;
 constexpr int kGemmTmemCols = 512;
-constexpr int kGemmAccCol = 0;   // two accumulators: columns [0, 256)
-constexpr int kGemmACol = 256;   // A buffers: columns [256, 256 + 6 * 32)
+constexpr int kGemmAccCol = 0;   // accumulators: columns [0, kGemmAccBufs * kGemmTok)
+constexpr int kGemmACol = 256;   // A buffers: columns [256, 256 + stages * 32)
 
 struct GemmParams {
   float *y;
@@ -391,8 +397,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t bbase = smem_u32(smem + L.bstage);
       long long c = 0, tc = 0;
       for (long long t = blockIdx.x; t < p.tiles && !*abort_flag; t += gridDim.x, ++tc) {
-        const int a = (int)(tc & 1);
-        if (tc >= 2) wait(&accempty[a], (uint32_t)(((tc >> 1) - 1) & 1));
+        const int a = (int)(tc % kGemmAccBufs);
+        if (tc >= kGemmAccBufs) wait(&accempty[a], (uint32_t)(((tc / kGemmAccBufs) - 1) & 1));
         tc_fence_after();
         const uint32_t d_tmem = tmem + kGemmAccCol + a * kGemmTok;
         for (int kb = 0; kb < p.NKB && !*abort_flag; ++kb, ++c) {
@@ -477,8 +483,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     long long tc = 0;
     for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x, ++tc) {
       const int rt = (int)(t % p.NRT), tt = (int)(t / p.NRT);
-      const int a = (int)(tc & 1);
-      wait(&accfull[a], (uint32_t)((tc >> 1) & 1));
+      const int a = (int)(tc % kGemmAccBufs);
+      wait(&accfull[a], (uint32_t)((tc / kGemmAccBufs) & 1));
       if (__any_sync(0xffffffffu, *abort_flag)) break;  // tcgen05.ld is warp-collective
       tc_fence_after();
       const int64_t n = (int64_t)rt * kGemmRows + row;

@@ -1,0 +1,257 @@
+// Decode-path W2A8 ternary GEMV for 3..16 tokens on the mma.sync tensor path.
+//
+// Same operation as the other GEMV kernels: y[m, n] = (sum_k (code[n,k]-1) *
+// x_q[m,k]) * (w_scale * s_m / 127), the integer-domain product of BitNet
+// 深度拆解 §3.1 (§1: a ternary weight turns each product into +x, 0 or -x)
+// with the dequantisation of §2.3.
+//
+// A few tokens need 2 * M multiply-adds per weight: more than dp4a sustains
+// at HBM speed for M > 2, while tcgen05 MMAs with N = 8..16 tokens cost far
+// more per instruction than their arithmetic (measured).  mma.sync m16n8k16
+// takes A (16 weight rows x 16 K) straight from registers, so decoding costs
+// one AND per two weights and nothing else touches shared memory but the
+// packed weights and the activations:
+//   * A fragment: a 2-bit field masked in place inside a 16-bit lane is the
+//     fp16 subnormal code * 4^i * 2^-24; B is the prepared activation matrix
+//     (x_q * 4^-i in fp16, gemm_prep_kernel), so every product is
+//     code * x * 2^-24 and fp32 accumulation is exact (D * 2^24 is the
+//     integer sum of code * x; the per-token sum of x_q is subtracted once).
+//   * Work units are (128-row tile, 512-K chunk) pairs; CTA c takes an equal
+//     contiguous range of units (stream-K).  Each unit's 16 KB of packed
+//     weights (TMA, 128-byte swizzle) and its activation slice arrive in one
+//     stage of a ring (up to kMmaStages in flight, weights requested before
+//     waiting on the previous kernel).
+//   * Warp w of the 8 compute warps takes the 64-K column w of every unit for
+//     all 8 row blocks: its activation fragments are loaded once per unit and
+//     reused 8 times.  At the end of a row tile's segment the warps add their
+//     exact int32 partial sums in shared memory; a tile finished inside the
+//     CTA is written directly, a tile split between CTAs is summed with int32
+//     atomics in the workspace and written by the CTA that completes it
+//     (ticket), which re-zeroes the entries.
+// Every wait is bounded; on expiry the CTA records the error and walks out
+// without waiting (outputs undefined, the device error word says so).
+#pragma once
+
+#include "common.cuh"
+#include "gemv_tc.cuh"
+
+namespace bitnet {
+
+constexpr int kMmaWarps = 8;                 // compute warps (one 64-K column each)
+constexpr int kMmaThreads = (kMmaWarps + 1) * 32;
+constexpr int kMmaStages = 5;
+constexpr int kMmaBar = 3;                   // named barrier of the compute warps
+
+template <int NT8>
+struct GemvMmaSmem {
+  static constexpr int kTok = NT8 * 8;                  // token rows of the B box
+  static constexpr int kBBytes = 8 * kTok * 128;        // activation slice of a unit
+  static constexpr int kStage = 16384 + kBBytes;
+  static constexpr int ring = 0;
+  static constexpr int red = kMmaStages * kStage;       // [128 rows][M] int32
+  static constexpr int bars = red + 128 * 16 * 4;
+  static constexpr int flags = bars + 2 * kMmaStages * 8;
+  static constexpr int bytes = flags + 16;
+};
+
+template <int NT8>
+__global__ void __launch_bounds__(kMmaThreads, 1)
+    gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap bmap,
+                    const GemvTcParams p) {
+  using L = GemvMmaSmem<NT8>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bars);
+  uint64_t *empty = full + kMmaStages;
+  int32_t *red = reinterpret_cast<int32_t *>(smem + L::red);
+  volatile int *flags = reinterpret_cast<volatile int *>(smem + L::flags);  // [0] abort, [1] last CTA
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const long long g0 = p.units * blockIdx.x / gridDim.x;
+  const long long g1 = p.units * (blockIdx.x + 1) / gridDim.x;
+  pdl_launch_dependents();
+  if (tid == 0) {
+    for (int i = 0; i < kMmaStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kMmaWarps);
+    }
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbar_init();
+  }
+  for (int i = tid; i < 128 * p.M; i += kMmaThreads) red[i] = 0;
+  __syncthreads();
+
+  if (warp == kMmaWarps) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      prefetch_tensormap(&wmap);
+      prefetch_tensormap(&bmap);
+      const uint64_t pol_w = l2_policy_evict_first(), pol_b = l2_policy_evict_last();
+      long long it = 0;
+      bool waited = false;
+      for (long long u = g0; u < g1; ++u, ++it) {
+        const int s = (int)(it % kMmaStages);
+        if (it >= kMmaStages && !mbar_wait(&empty[s], (uint32_t)(((it / kMmaStages) - 1) & 1))) {
+          raise_device_error(kDevErrTimeout);
+          flags[0] = 1;
+        }
+        if (flags[0]) break;
+        const int r = (int)(u / p.NCH), c = (int)(u % p.NCH);
+        const int nkb = tc_chunk_kbs(p, c);
+        uint8_t *st = smem + L::ring + s * L::kStage;
+        mbar_arrive_expect_tx(&full[s], 16384 + nkb * L::kTok * 128);
+        tma_load_2d(st, &wmap, &full[s], c * 128, r * 128, pol_w);
+        if (!waited) {  // the activations come from the previous kernel
+          pdl_wait_prior_grid();
+          waited = true;
+        }
+        for (int kb = 0; kb < nkb; ++kb)
+          tma_load_2d(st + 16384 + kb * L::kTok * 128, &bmap, &full[s], (c * 8 + kb) * kTcKB, 0, pol_b);
+      }
+      if (!waited) pdl_wait_prior_grid();
+      if (flags[0]) {  // leave no copy in flight (bounded waits)
+        for (long long j = (it > kMmaStages ? it - kMmaStages : 0); j < it; ++j)
+          mbar_wait(&full[j % kMmaStages], (uint32_t)((j / kMmaStages) & 1));
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------- compute warps --
+  pdl_wait_prior_grid();  // xsum / fscale come from the previous kernel
+  const int g = lane >> 2, t = lane & 3;
+  const int kb = warp;  // this warp's 64-K column of every unit
+  float d[8][NT8][4];
+#pragma unroll
+  for (int rb = 0; rb < 8; ++rb)
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d[rb][nt][e] = 0.0f;
+
+  long long it = 0;
+  long long u = g0;
+  while (u < g1) {
+    const int r = (int)(u / p.NCH);
+    const int c0 = (int)(u % p.NCH);
+    const long long tile_end = (long long)(r + 1) * p.NCH;
+    const long long u_end = tile_end < g1 ? tile_end : g1;  // segment: units [u, u_end) of tile r
+    const int nch = (int)(u_end - u);
+    for (; u < u_end; ++u, ++it) {
+      const int s = (int)(it % kMmaStages);
+      if (!flags[0] && !mbar_wait(&full[s], (uint32_t)((it / kMmaStages) & 1))) {
+        raise_device_error(kDevErrTimeout);
+        flags[0] = 1;
+      }
+      const int c = (int)(u % p.NCH);
+      if (kb < tc_chunk_kbs(p, c)) {
+        const uint32_t st = smem_u32(smem + L::ring + s * L::kStage);
+        uint32_t w0[8], w1[8];
+#pragma unroll
+        for (int rb = 0; rb < 8; ++rb) {
+          const int r0 = rb * 16 + g;  // r0 & 7 == g, (r0 + 8) & 7 == g
+          const uint32_t off = (uint32_t)((((kb ^ g) & 7) << 4) + (t << 2));
+          w0[rb] = lds_u32(st + r0 * 128 + off);
+          w1[rb] = lds_u32(st + (r0 + 8) * 128 + off);
+        }
+        const uint32_t bst = st + 16384 + kb * L::kTok * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t b0[NT8], b1[NT8];
+#pragma unroll
+          for (int nt = 0; nt < NT8; ++nt) {
+            const int tok = nt * 8 + g;
+            const int ci = t * 2 + (j >> 1);  // 16-byte chunk of the 128-byte activation row
+            const uint2 bv = lds_u64(bst + tok * 128 + (((ci ^ (tok & 7)) & 7) << 4) + ((j & 1) << 3));
+            b0[nt] = bv.x;
+            b1[nt] = bv.y;
+          }
+#pragma unroll
+          for (int rb = 0; rb < 8; ++rb) {
+            uint32_t a0, a1, a2, a3;
+            if (j < 3) {
+              const uint32_t m0 = 0x00030003u << (4 * j), m1 = 0x00030003u << (4 * j + 2);
+              a0 = w0[rb] & m0;
+              a1 = w1[rb] & m0;
+              a2 = w0[rb] & m1;
+              a3 = w1[rb] & m1;
+            } else {
+              const uint32_t h0 = w0[rb] >> 12, h1 = w1[rb] >> 12;
+              a0 = h0 & 0x00030003u;
+              a1 = h1 & 0x00030003u;
+              a2 = h0 & 0x000C000Cu;
+              a3 = h1 & 0x000C000Cu;
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT8; ++nt) mma_f16_16816(d[rb][nt], a0, a1, a2, a3, b0[nt], b1[nt]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    // ------------------------------------------------------- segment end --
+    // exact int32 partial sums of this warp's column into red[row][token]
+#pragma unroll
+    for (int rb = 0; rb < 8; ++rb)
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int row = rb * 16 + g + ((e >> 1) << 3);
+          const int tok = nt * 8 + 2 * t + (e & 1);
+          const int v = __float2int_rn(d[rb][nt][e] * 16777216.0f);
+          d[rb][nt][e] = 0.0f;
+          if (tok < p.M && v != 0) atomicAdd(&red[row * p.M + tok], v);
+        }
+    named_barrier_sync(kMmaBar, kMmaWarps * 32);
+    const bool whole = (c0 == 0) && (nch == p.NCH);
+    const int entries = 128 * p.M;
+    if (whole) {
+      for (int i = tid; i < entries; i += kMmaWarps * 32) {
+        const int row = i / p.M, tok = i % p.M;
+        const int64_t n = (int64_t)r * 128 + row;
+        const int32_t v = red[i];
+        red[i] = 0;
+        if (n < p.N) {
+          const int32_t o = v - __ldg(p.xsum + tok);
+          if (p.acc) p.acc[(int64_t)tok * p.N + n] = o;
+          p.y[(int64_t)tok * p.N + n] = __fmul_rn((float)o, __ldg(p.fscale + tok));
+        }
+      }
+    } else {
+      for (int i = tid; i < entries; i += kMmaWarps * 32) {
+        const int row = i / p.M, tok = i % p.M;
+        const int64_t n = (int64_t)r * 128 + row;
+        const int32_t v = red[i];
+        red[i] = 0;
+        if (n < p.N && v != 0) atomicAdd(&p.ws_partial[n * p.M + tok], v);
+      }
+      __threadfence();  // partial sums visible before the ticket
+      named_barrier_sync(kMmaBar, kMmaWarps * 32);
+      if (tid == 0) {
+        const unsigned old = atomicAdd(&p.ws_ticket[r], (unsigned)nch);
+        flags[1] = (old + (unsigned)nch == (unsigned)p.NCH) ? 1 : 0;
+      }
+      named_barrier_sync(kMmaBar, kMmaWarps * 32);
+      if (flags[1]) {
+        __threadfence();
+        for (int i = tid; i < entries; i += kMmaWarps * 32) {
+          const int row = i / p.M, tok = i % p.M;
+          const int64_t n = (int64_t)r * 128 + row;
+          if (n < p.N) {
+            const int32_t o = atomicExch(&p.ws_partial[n * p.M + tok], 0) - __ldg(p.xsum + tok);
+            if (p.acc) p.acc[(int64_t)tok * p.N + n] = o;
+            p.y[(int64_t)tok * p.N + n] = __fmul_rn((float)o, __ldg(p.fscale + tok));
+          }
+        }
+        if (tid == 0) atomicExch(&p.ws_ticket[r], 0u);
+      }
+    }
+    named_barrier_sync(kMmaBar, kMmaWarps * 32);
+  }
+}
+
+}  // namespace bitnet

@@ -48,17 +48,20 @@
 namespace bitnet {
 
 #ifndef BITNET_TC_DEC_SETS
-#define BITNET_TC_DEC_SETS 2
+#define BITNET_TC_DEC_SETS 1
 #endif
 constexpr int kTcDecSets = BITNET_TC_DEC_SETS;  // decoder warp sets of 4 warps
 constexpr int kTcThreads = 384 + (kTcDecSets - 1) * 128;
+// Two CTAs per SM (half the TMEM and shared memory each): two MMA issuers
+// per SM measured 1.35x the throughput of one.
+constexpr int kTcCtasPerSm = 2;
 constexpr int kTcRows = 128;       // weight rows per tile (MMA M)
 constexpr int kTcChunkK = 512;     // K per work unit (one 128-byte column of packed rows)
 constexpr int kTcKB = 64;          // K per MMA step group (4 MMAs of K = 16)
-constexpr int kTcWStages = 6;      // packed-weight stages (16 KB each)
-constexpr int kTcStages = 8;       // activation stages in smem == A buffers in TMEM
-constexpr int kTcTmemCols = 512;
-constexpr int kTcACol = 128;       // A buffers: columns [128, 128 + 8 * 32)
+constexpr int kTcWStages = 3;      // packed-weight stages (16 KB each)
+constexpr int kTcStages = 4;       // activation stages in smem == A buffers in TMEM
+constexpr int kTcTmemCols = 256;   // per CTA (two CTAs per SM)
+constexpr int kTcACol = 128;       // A buffers: columns [128, 128 + 4 * 32)
 constexpr int kTcEpiBar = 2;       // named barrier of the epilogue warps
 
 struct GemvTcParams {
@@ -92,7 +95,7 @@ struct GemvTcSmem {
 __device__ __forceinline__ int tc_chunk_kbs(const GemvTcParams &p, int c) { return min(8, p.NKB - 8 * c); }
 
 template <int NT>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap bmap,
                    const GemvTcParams p) {
   using L = GemvTcSmem<NT>;
