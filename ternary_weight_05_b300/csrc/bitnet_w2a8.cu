@@ -127,6 +127,10 @@ struct GemvPlan {
   size_t ws_partial_bytes, ws_zero_bytes, ws_prep_xb, ws_prep_sums, ws_bytes;
 };
 
+// Token rows of the prepared activations of the mma.sync GEMV (3..16
+// tokens: padded to 8 or 16, K-block-major); 0 for the other kernels.
+int gemv_mma_rows(int64_t M) { return (M >= 3 && M <= 16) ? (M <= 8 ? 8 : 16) : 0; }
+
 GemvPlan plan_gemv(int64_t M, int64_t N, int64_t K, int sms) {
   GemvPlan pl = {};
   pl.NR = (int)cdiv(N, kStageRows);
@@ -144,7 +148,7 @@ GemvPlan plan_gemv(int64_t M, int64_t N, int64_t K, int sms) {
   pl.ws_partial_bytes = (size_t)pl.NR * kStageRows * M * 4;
   pl.ws_zero_bytes = ((pl.ws_partial_bytes + (size_t)pl.NR * 4) + 255) & ~(size_t)255;
   pl.ws_prep_xb = pl.ws_zero_bytes;
-  pl.ws_prep_sums = pl.ws_prep_xb + gemm_xb_bytes(M, K);
+  pl.ws_prep_sums = pl.ws_prep_xb + gemm_xb_bytes(std::max<int64_t>(M, gemv_mma_rows(M)), K);
   pl.ws_bytes = pl.ws_prep_sums + (((size_t)M * 8 + 255) & ~(size_t)255) + 256;
   return pl;
 }
@@ -190,7 +194,8 @@ bitnet_status launch_quant(const T *x, bool vec, int64_t M, int64_t K, int8_t *x
 // Prep grid for the tensor-core GEMV: M token CTAs plus CTAs that zero the
 // split-tile partials and tickets (32 KB each).
 unsigned prep_grid(int64_t M, const GemvPlan &pl) {
-  return (unsigned)(M + std::min<int64_t>(148, cdiv((int64_t)pl.ws_zero_bytes, 32768)));
+  return (unsigned)(std::max<int64_t>(M, gemv_mma_rows(M)) +
+                    std::min<int64_t>(148, cdiv((int64_t)pl.ws_zero_bytes, 32768)));
 }
 
 // The streaming-load kernel takes one or two tokens whose activation words
@@ -292,17 +297,28 @@ bitnet_status launch_gemv_tc(const int8_t *x_q, const float *scale, int64_t M, c
   uint32_t *xb = reinterpret_cast<uint32_t *>(ws + pl.ws_prep_xb);
   int32_t *xsum = reinterpret_cast<int32_t *>(ws + pl.ws_prep_sums);
   float *fscale = reinterpret_cast<float *>(ws + pl.ws_prep_sums + (size_t)M * 4);
+  // 3..16 tokens: mma.sync kernel (8 or 16 token rows, K-block-major
+  // activations: one box per unit); 17..64: tcgen05 kernel
+  const bool mma = M <= 16;
+  const int NT = mma ? gemv_mma_rows(M) : (M <= 32 ? 32 : 64);
   if (x_q) {
     bitnet_status st = launch(gemm_prep_kernel, dim3(prep_grid(M, pl)), dim3(256), 0, stream, x_q, scale, w_scale,
-                              K, xb, xsum, fscale, M, static_cast<uint4 *>(workspace), (int64_t)(pl.ws_zero_bytes / 16));
+                              K, xb, xsum, fscale, M, static_cast<uint4 *>(workspace), (int64_t)(pl.ws_zero_bytes / 16),
+                              mma ? NT : 0);
     if (st) return st;
   }
-  // 3..16 tokens: mma.sync kernel (8 or 16 token rows); 17..64: tcgen05 kernel
-  const bool mma = M <= 16;
-  const int NT = mma ? (M <= 8 ? 8 : 16) : (M <= 32 ? 32 : 64);
   CUtensorMap wmap, bmap;
   if (bitnet_status s = encode_packed_map(&wmap, packed, N, K, 128, kTcRows, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
-  {
+  if (mma) {
+    cuuint64_t dims[2] = {(cuuint64_t)kTcKB, (cuuint64_t)(K / kTcKB) * (cuuint64_t)NT};
+    cuuint64_t strides[1] = {(cuuint64_t)kTcKB * 2};
+    cuuint32_t box[2] = {kTcKB, (cuuint32_t)(8 * NT)};
+    cuuint32_t estr[2] = {1, 1};
+    if (g_encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xb, dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return BITNET_ERR_CUDA;
+  } else {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     cuuint32_t box[2] = {kTcKB, (cuuint32_t)NT};
@@ -566,7 +582,7 @@ int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uin
   float *fscale = reinterpret_cast<float *>(ws + gemm_xb_bytes(M, K) + (size_t)M * 4);
 
   bitnet_status st = launch(gemm_prep_kernel, dim3((unsigned)M), dim3(256), 0, stream, x_q, scale, w_scale, K,
-                            xb, xsum, fscale, M, static_cast<uint4 *>(nullptr), (int64_t)0);
+                            xb, xsum, fscale, M, static_cast<uint4 *>(nullptr), (int64_t)0, 0);
   if (st) return st;
   return launch_gemm_tc(xb, xsum, fscale, M, packed, N, K, y, acc, d, stream);
 }
@@ -694,11 +710,13 @@ int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed,
     const dim3 pgrid = gemv ? dim3(prep_grid(M, pl)) : dim3((unsigned)M);
     uint4 *zero = gemv ? static_cast<uint4 *>(workspace) : nullptr;
     const int64_t zero_n16 = gemv ? (int64_t)(pl.ws_zero_bytes / 16) : 0;
+    const int trows = gemv ? gemv_mma_rows(M) : 0;
     bitnet_status st =
         bf ? launch(fused_prep_kernel<__nv_bfloat16>, pgrid, dim3(256), 0, stream,
-                    static_cast<const __nv_bfloat16 *>(x), w_scale, K, xb, xsum, fscale, x_q, scale, M, zero, zero_n16)
+                    static_cast<const __nv_bfloat16 *>(x), w_scale, K, xb, xsum, fscale, x_q, scale, M, zero, zero_n16,
+                    trows)
            : launch(fused_prep_kernel<float>, pgrid, dim3(256), 0, stream, static_cast<const float *>(x), w_scale, K,
-                    xb, xsum, fscale, x_q, scale, M, zero, zero_n16);
+                    xb, xsum, fscale, x_q, scale, M, zero, zero_n16, trows);
     if (st) return st;
     if (M <= BITNET_GEMV_MAX_M)
       return launch_gemv_tc(nullptr, nullptr, M, packed, w_scale, N, K, y, acc, workspace, pl, d, stream);

@@ -185,12 +185,29 @@ __device__ __forceinline__ int prep_group(const int8_t (&v)[16], uint32_t *out) 
   return sum;
 }
 
-// CTAs past the M token rows of a prep kernel zero `zero` (n16 16-byte
-// words: the split-tile partial sums and tickets of the GEMV that follows),
-// after the previous kernel, which may share the workspace, has finished.
-__device__ __forceinline__ void prep_zero_tail(int64_t M, uint4 *zero, int64_t n16) {
-  const int64_t cta = (int64_t)blockIdx.x - M, nct = (int64_t)gridDim.x - M;
+// CTAs from `first` on zero `zero` (n16 16-byte words: the split-tile
+// partial sums and tickets of the GEMV that follows), after the previous
+// kernel, which may share the workspace, has finished.
+__device__ __forceinline__ void prep_zero_tail(int64_t first, uint4 *zero, int64_t n16) {
+  const int64_t cta = (int64_t)blockIdx.x - first, nct = (int64_t)gridDim.x - first;
   for (int64_t i = cta * 256 + threadIdx.x; i < n16; i += nct * 256) zero[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Where 16-K group q of token m goes in the prepared activations.  T == 0:
+// row-major [M][K].  T > 0: K-block-major [K/64][T][64], T token rows per
+// 64-K block (rows >= M are zero), so the 8 K-blocks of a 512-K chunk are
+// one contiguous box of 8*T rows of 128 bytes.
+__device__ __forceinline__ uint32_t *prep_out(uint32_t *xb, int64_t m, int64_t q, int64_t K, int T) {
+  return T == 0 ? xb + m * (K / 2) + q * 8 : xb + ((q >> 2) * T + m) * 32 + (q & 3) * 8;
+}
+
+// Zero rows M..T-1 of the K-block-major layout (CTAs M..T-1 of a prep grid).
+__device__ __forceinline__ void prep_zero_row(uint32_t *xb, int64_t m, int64_t K, int T) {
+  for (int64_t q = threadIdx.x; q < K / 16; q += 256) {
+    uint4 *dst = reinterpret_cast<uint4 *>(prep_out(xb, m, q, K, T));
+    dst[0] = make_uint4(0u, 0u, 0u, 0u);
+    dst[1] = make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 // x_q int8 [M, K] -> fp16 B matrix [M, K] (per 16-K group, element 2i+h is
@@ -201,23 +218,27 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const int8_t *__restrict
                                                         const float *__restrict__ w_scale, int64_t K,
                                                         uint32_t *__restrict__ xb, int32_t *__restrict__ xsum,
                                                         float *__restrict__ fscale, int64_t M, uint4 *zero,
-                                                        int64_t zero_n16) {
+                                                        int64_t zero_n16, int T) {
   pdl_launch_dependents();
   pdl_wait_prior_grid();
+  const int64_t rows = M > T ? M : T;
+  if ((int64_t)blockIdx.x >= rows) {
+    prep_zero_tail(rows, zero, zero_n16);
+    return;
+  }
   if ((int64_t)blockIdx.x >= M) {
-    prep_zero_tail(M, zero, zero_n16);
+    prep_zero_row(xb, blockIdx.x, K, T);
     return;
   }
   __shared__ int red[8];
   const int64_t m = blockIdx.x;
   const int8_t *row = xq + m * K;
-  uint32_t *out = xb + m * (K / 2);
   int sum = 0;
   for (int64_t q = threadIdx.x; q < K / 16; q += 256) {
     const int4 u = *reinterpret_cast<const int4 *>(row + q * 16);
     int8_t v[16];
     memcpy(v, &u, 16);
-    sum += prep_group(v, out + q * 8);
+    sum += prep_group(v, prep_out(xb, m, q, K, T));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -241,18 +262,22 @@ __global__ void __launch_bounds__(256)
     fused_prep_kernel(const T *__restrict__ x, const float *__restrict__ w_scale, int64_t K,
                       uint32_t *__restrict__ xb, int32_t *__restrict__ xsum, float *__restrict__ fscale,
                       int8_t *__restrict__ xq_out, float *__restrict__ scale_out, int64_t M, uint4 *zero,
-                      int64_t zero_n16) {
+                      int64_t zero_n16, int TR) {
   pdl_launch_dependents();
   pdl_wait_prior_grid();
+  const int64_t rows = M > TR ? M : TR;
+  if ((int64_t)blockIdx.x >= rows) {
+    prep_zero_tail(rows, zero, zero_n16);
+    return;
+  }
   if ((int64_t)blockIdx.x >= M) {
-    prep_zero_tail(M, zero, zero_n16);
+    prep_zero_row(xb, blockIdx.x, K, TR);
     return;
   }
   __shared__ float redf[8];
   __shared__ int red[8];
   const int64_t m = blockIdx.x;
   const T *row = x + m * K;
-  uint32_t *out = xb + m * (K / 2);
   float amax = 0.0f;
   for (int64_t k = (int64_t)threadIdx.x * 8; k < K; k += 256 * 8) {
     float v[8];
@@ -278,7 +303,7 @@ __global__ void __launch_bounds__(256)
       memcpy(&u, v, 16);
       *reinterpret_cast<int4 *>(xq_out + m * K + q * 16) = u;
     }
-    sum += prep_group(v, out + q * 8);
+    sum += prep_group(v, prep_out(xb, m, q, K, TR));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);

@@ -18,9 +18,10 @@
 //     integer sum of code * x; the per-token sum of x_q is subtracted once).
 //   * Work units are (128-row tile, 512-K chunk) pairs; CTA c takes an equal
 //     contiguous range of units (stream-K).  Each unit's 16 KB of packed
-//     weights (TMA, 128-byte swizzle) and its activation slice arrive in one
-//     stage of a ring (up to kMmaStages in flight, weights requested before
-//     waiting on the previous kernel).
+//     weights and its activation slice (prepared K-block-major, so the slice
+//     is one box) arrive in one stage of a ring with two TMA copies (the cost
+//     of a copy is per box, so boxes are few and large); up to kMmaStages in
+//     flight, weights requested before waiting on the previous kernel.
 //   * Warp w of the 8 compute warps takes the 64-K column w of every unit for
 //     all 8 row blocks: its activation fragments are loaded once per unit and
 //     reused 8 times.  At the end of a row tile's segment the warps add their
@@ -98,16 +99,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
         if (flags[0]) break;
         const int r = (int)(u / p.NCH), c = (int)(u % p.NCH);
-        const int nkb = tc_chunk_kbs(p, c);
         uint8_t *st = smem + L::ring + s * L::kStage;
-        mbar_arrive_expect_tx(&full[s], 16384 + nkb * L::kTok * 128);
+        mbar_arrive_expect_tx(&full[s], 16384 + L::kBBytes);
         tma_load_2d(st, &wmap, &full[s], c * 128, r * 128, pol_w);
         if (!waited) {  // the activations come from the previous kernel
           pdl_wait_prior_grid();
           waited = true;
         }
-        for (int kb = 0; kb < nkb; ++kb)
-          tma_load_2d(st + 16384 + kb * L::kTok * 128, &bmap, &full[s], (c * 8 + kb) * kTcKB, 0, pol_b);
+        // the unit's 8 K-blocks x kTok token rows: one box (rows past K are zero-filled)
+        tma_load_2d(st + 16384, &bmap, &full[s], 0, c * 8 * L::kTok, pol_b);
       }
       if (!waited) pdl_wait_prior_grid();
       if (flags[0]) {  // leave no copy in flight (bounded waits)
