@@ -49,6 +49,8 @@ def _load():
         "oracle_quant_act": (None, [_p, _i64, _i64, _p, _p]),
         "oracle_contract": (None, [_p, _p, _i64, _i64, _i64, _i64, _i64, _p]),
         "oracle_epilogue": (None, [_p, _p, _f32, _i64, _i64, _p]),
+        "oracle_swiglu": (None, [_p, _p, _p, _f32, _f32, _i64, _i64, _p]),
+        "oracle_silu": (ctypes.c_double, [ctypes.c_double]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -174,3 +176,29 @@ def bitlinear(x: np.ndarray, packed: np.ndarray, beta: float, N: int, K: int, th
     xq, s = quant_act(x)
     acc = contract(xq, packed, N, K, threads=threads)
     return epilogue(acc, s, beta), acc, xq, s
+
+
+def silu(z: float) -> float:
+    return float(_load().oracle_silu(float(z)))
+
+
+def swiglu(acc_gate: np.ndarray, acc_up: np.ndarray, scale: np.ndarray, w_scale_gate: float,
+           w_scale_up: float) -> np.ndarray:
+    """fp64 [M, I]: silu(y_gate) * y_up from the exact BitLinear outputs."""
+    acc_gate = np.ascontiguousarray(acc_gate, dtype=np.int32)
+    acc_up = np.ascontiguousarray(acc_up, dtype=np.int32)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    M, I = acc_gate.shape
+    assert acc_up.shape == (M, I)
+    out = np.empty((M, I), dtype=np.float64)
+    _load().oracle_swiglu(_ptr(acc_gate), _ptr(acc_up), _ptr(scale), w_scale_gate, w_scale_up, M, I, _ptr(out))
+    return out
+
+
+def bitlinear_swiglu(x: np.ndarray, packed_gate: np.ndarray, beta_gate: float, packed_up: np.ndarray,
+                     beta_up: float, I: int, K: int, threads: int = 1):
+    """The FFN front half: quant_act -> two contractions -> silu(gate) * up (fp64)."""
+    xq, s = quant_act(x)
+    acc_g = contract(xq, packed_gate, I, K, threads=threads)
+    acc_u = contract(xq, packed_up, I, K, threads=threads)
+    return swiglu(acc_g, acc_u, s, beta_gate, beta_up), acc_g, acc_u, xq, s

@@ -187,3 +187,23 @@ void oracle_epilogue(const int32_t *acc, const float *scale, float w_scale, int6
       y[m * N + n] =
           (float)((double)acc[m * N + n] * (double)w_scale * (double)scale[m] / 127.0);
 }
+
+/* SwiGLU feed-forward product of the BitTransformer block ([Deep-dive]
+ * section 3.1: down(F.silu(gate(h)) * up(h))): for the two BitLinear outputs
+ * of the same activations, a = silu(y_gate) * y_up with silu(z) = z * sigmoid(z)
+ * = z / (1 + exp(-z)).  The BitLinear outputs are taken exactly, in fp64, from
+ * the integer accumulators (acc * w_scale * s_m / 127, not rounded to fp32),
+ * and the product is returned in fp64: the reference value the fp32 GPU result
+ * is compared with.  acc_gate / acc_up are [M, I]. */
+void oracle_swiglu(const int32_t *acc_gate, const int32_t *acc_up, const float *scale, float w_scale_gate,
+                   float w_scale_up, int64_t M, int64_t I, double *out) {
+  for (int64_t m = 0; m < M; m++)
+    for (int64_t i = 0; i < I; i++) {
+      double yg = (double)acc_gate[m * I + i] * (double)w_scale_gate * (double)scale[m] / 127.0;
+      double yu = (double)acc_up[m * I + i] * (double)w_scale_up * (double)scale[m] / 127.0;
+      out[m * I + i] = yg / (1.0 + exp(-yg)) * yu;
+    }
+}
+
+/* silu(z) in fp64, the same definition, for the pins. */
+double oracle_silu(double z) { return z / (1.0 + exp(-z)); }

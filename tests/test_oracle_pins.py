@@ -326,3 +326,51 @@ def test_bitlinear_forward_matches_page_torch_formulation(oracle_mod):
     tmean = torch.from_numpy(W).abs().mean()
     tq = torch.clamp(torch.round((1.0 / (1.0 * tmean + 1e-8)) * torch.from_numpy(W)), -1, 1)
     assert np.array_equal(tq.numpy().astype(np.int8), wt.numpy().astype(np.int8))
+
+
+# ------------------------------------------------ SwiGLU (FFN, next row) ---
+
+def test_silu_special_values(oracle_mod):
+    # sigmoid(ln 3) = 1 / (1 + 1/3) = 3/4, so silu(+-ln 3) = +-ln 3 * {3/4, 1/4}:
+    # a dropped minus sign in exp(-z) swaps the two values
+    ln3 = np.log(3.0)
+    assert oracle_mod.silu(ln3) == pytest.approx(0.75 * ln3, rel=1e-15)
+    assert oracle_mod.silu(-ln3) == pytest.approx(-0.25 * ln3, rel=1e-15)
+    assert oracle_mod.silu(0.0) == 0.0
+    assert oracle_mod.silu(60.0) == 60.0  # sigmoid rounds to 1
+    assert -1e-20 < oracle_mod.silu(-60.0) < 0.0
+
+
+def test_silu_odd_part_is_identity(oracle_mod):
+    # silu(z) - silu(-z) = z (sigmoid(z) + sigmoid(-z) = 1)
+    for z in np.linspace(-30.0, 30.0, 241):
+        assert oracle_mod.silu(z) - oracle_mod.silu(-z) == pytest.approx(z, abs=1e-12)
+
+
+def test_swiglu_uses_exact_bitlinear_outputs(oracle_mod):
+    # acc * w_scale * s / 127 with s = 127, w_scale = 1 is the accumulator itself
+    acc_g = np.array([[0, 3, -3, 40]], dtype=np.int32)
+    acc_u = np.array([[5, 2, 2, -1]], dtype=np.int32)
+    out = oracle_mod.swiglu(acc_g, acc_u, np.array([127.0], np.float32), 1.0, 1.0)
+    expect = [0.0, 2 * oracle_mod.silu(3.0), 2 * oracle_mod.silu(-3.0), -oracle_mod.silu(40.0)]
+    assert np.allclose(out[0], expect, rtol=1e-15, atol=0)
+    # gate and up scales enter separately
+    out2 = oracle_mod.swiglu(acc_g, acc_u, np.array([127.0], np.float32), 0.5, 2.0)
+    assert out2[0, 1] == pytest.approx(oracle_mod.silu(1.5) * 4.0, rel=1e-15)
+
+
+def test_bitlinear_swiglu_matches_two_bitlinears(oracle_mod):
+    rng = np.random.default_rng(3)
+    I, K = 20, 64
+    Wg = rng.normal(0, 0.02, (I, K)).astype(np.float32)
+    Wu = rng.normal(0, 0.02, (I, K)).astype(np.float32)
+    pg, bg, _ = oracle_mod.pack_weights(Wg)
+    pu, bu, _ = oracle_mod.pack_weights(Wu)
+    x = rng.normal(0, 1, (2, K)).astype(np.float32)
+    out, acc_g, acc_u, _, s = oracle_mod.bitlinear_swiglu(x, pg, bg, pu, bu, I, K)
+    yg, acc_g2, _, _ = oracle_mod.bitlinear(x, pg, bg, I, K)
+    yu, acc_u2, _, _ = oracle_mod.bitlinear(x, pu, bu, I, K)
+    assert np.array_equal(acc_g, acc_g2) and np.array_equal(acc_u, acc_u2)
+    # the fp32 BitLinear outputs are within one rounding of the exact ones
+    ref = np.array([[oracle_mod.silu(float(a)) * float(b) for a, b in zip(ra, rb)] for ra, rb in zip(yg, yu)])
+    assert np.allclose(out, ref, rtol=1e-5, atol=1e-12)
