@@ -51,6 +51,9 @@ def _load():
         "oracle_epilogue": (None, [_p, _p, _f32, _i64, _i64, _p]),
         "oracle_swiglu": (None, [_p, _p, _p, _f32, _f32, _i64, _i64, _p]),
         "oracle_silu": (ctypes.c_double, [ctypes.c_double]),
+        "oracle_pack_weights_grouped": (None, [_p, _i64, _i64, _i64, _f32, _f32, _p, _p, _p]),
+        "oracle_contract_grouped": (None, [_p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
+        "oracle_epilogue_grouped": (None, [_p, _p, _p, _i64, _i64, _i64, _p, _p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -202,3 +205,63 @@ def bitlinear_swiglu(x: np.ndarray, packed_gate: np.ndarray, beta_gate: float, p
     acc_g = contract(xq, packed_gate, I, K, threads=threads)
     acc_u = contract(xq, packed_up, I, K, threads=threads)
     return swiglu(acc_g, acc_u, s, beta_gate, beta_up), acc_g, acc_u, xq, s
+
+
+def pack_weights_grouped(W: np.ndarray, G: int, alpha: float = 1.0, eps: float = 1e-8):
+    """Group-wise ternarisation: every G consecutive weights of a row are one
+    group with its own gamma and beta.  Returns (packed uint8 [N*K/4],
+    w_scale float32 [N, K/G] (beta per group), absmean float32 [N, K/G])."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    N, K = W.shape
+    assert G > 0 and G % 4 == 0 and K % G == 0
+    packed = np.empty(N * K // 4, dtype=np.uint8)
+    ws = np.empty((N, K // G), dtype=np.float32)
+    am = np.empty((N, K // G), dtype=np.float32)
+    _load().oracle_pack_weights_grouped(_ptr(W), N, K, G, alpha, eps, _ptr(packed), _ptr(ws), _ptr(am))
+    return packed, ws, am
+
+
+def contract_grouped(xq: np.ndarray, packed: np.ndarray, N: int, K: int, G: int, threads: int = 1) -> np.ndarray:
+    """int32 [M, N, K/G]: the integer product of each weight group."""
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    M = xq.shape[0]
+    assert xq.shape == (M, K) and packed.size * 4 >= N * K and K % G == 0
+    acc = np.empty((M, N, K // G), dtype=np.int32)
+    lib = _load()
+    if threads <= 1 or N < 2 * threads:
+        lib.oracle_contract_grouped(_ptr(xq), _ptr(packed), M, N, K, G, 0, N, _ptr(acc))
+        return acc
+    from concurrent.futures import ThreadPoolExecutor
+
+    bounds = np.linspace(0, N, threads + 1).astype(np.int64)
+    with ThreadPoolExecutor(threads) as ex:
+        futs = [ex.submit(lib.oracle_contract_grouped, _ptr(xq), _ptr(packed), M, N, K, G, int(a), int(b),
+                          _ptr(acc)) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+        for f in futs:
+            f.result()
+    return acc
+
+
+def epilogue_grouped(acc_g: np.ndarray, scale: np.ndarray, w_scale: np.ndarray):
+    """(y, cond), fp64 [M, N]: y = s/127 * sum_g w_scale[n, g] * acc_g, and
+    cond = s/127 * sum_g |w_scale[n, g] * acc_g| (the rounding condition)."""
+    acc_g = np.ascontiguousarray(acc_g, dtype=np.int32)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    w_scale = np.ascontiguousarray(w_scale, dtype=np.float32)
+    M, N, ng = acc_g.shape
+    assert w_scale.shape == (N, ng)
+    y = np.empty((M, N), dtype=np.float64)
+    cond = np.empty((M, N), dtype=np.float64)
+    _load().oracle_epilogue_grouped(_ptr(acc_g), _ptr(scale), _ptr(w_scale), M, N, ng, _ptr(y), _ptr(cond))
+    return y, cond
+
+
+def bitlinear_grouped(x: np.ndarray, packed: np.ndarray, w_scale: np.ndarray, N: int, K: int, G: int,
+                      threads: int = 1):
+    """BitLinear forward with group scales: quant_act -> per-group products
+    -> y (fp64), cond, acc_g, x_q, s."""
+    xq, s = quant_act(x)
+    acc_g = contract_grouped(xq, packed, N, K, G, threads=threads)
+    y, cond = epilogue_grouped(acc_g, s, w_scale)
+    return y, cond, acc_g, xq, s

@@ -207,3 +207,62 @@ void oracle_swiglu(const int32_t *acc_gate, const int32_t *acc_up, const float *
 
 /* silu(z) in fp64, the same definition, for the pins. */
 double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* Group-wise weight scales ([Deep-dive] section 4.3: in practice the weights
+ * are cut into groups of group_size -- commonly 128 -- and every group gets
+ * its own gamma and beta; one group per output row is the per-channel scale
+ * of [Hands-on] section 2.1).  Reading: a group is G consecutive weights of
+ * one output row, W[n, g*G .. g*G + G - 1] (G divides K, G % 4 == 0), so a
+ * row holds K / G groups; each group is ternarised exactly as a whole matrix
+ * is (oracle_pack_weights: mean|W_g| in the fixed fp64 order, gamma_g,
+ * codes, beta_g = nnz_g / G).  The packed bytes keep the row-major layout of
+ * the per-tensor format; w_scale[n * (K / G) + g] = beta_g and
+ * absmean[n * (K / G) + g] = mean|W_g|. */
+void oracle_pack_weights_grouped(const float *W, int64_t N, int64_t K, int64_t G, float alpha, float eps,
+                                 uint8_t *packed, float *w_scale, float *absmean) {
+  const int64_t ng = K / G;
+  for (int64_t n = 0; n < N; n++)
+    for (int64_t g = 0; g < ng; g++) {
+      const int64_t off = n * K + g * G; /* a multiple of 4: the group's bytes start at off / 4 */
+      oracle_pack_weights(W + off, 1, G, alpha, eps, packed + off / 4, &w_scale[n * ng + g], &absmean[n * ng + g]);
+    }
+}
+
+/* Per-group integer products: acc_g[(m * N + n) * (K / G) + g] =
+ * sum over k in group g of W_ternary[n, k] * x_q[m, k], rows n in
+ * [n_begin, n_end). */
+void oracle_contract_grouped(const int8_t *xq, const uint8_t *packed, int64_t M, int64_t N, int64_t K, int64_t G,
+                             int64_t n_begin, int64_t n_end, int32_t *acc_g) {
+  const int64_t ng = K / G;
+  for (int64_t n = n_begin; n < n_end; n++)
+    for (int64_t m = 0; m < M; m++)
+      for (int64_t g = 0; g < ng; g++) {
+        int64_t a = 0;
+        for (int64_t k = g * G; k < (g + 1) * G; k++) {
+          int64_t i = n * K + k;
+          int w = ((packed[i / 4] >> (2 * (i % 4))) & 3) - 1;
+          a += (int64_t)w * (int64_t)xq[m * K + k];
+        }
+        acc_g[(m * N + n) * ng + g] = (int32_t)a;
+      }
+}
+
+/* Dequantisation with group scales: y[m, n] = (s_m / 127) * sum_g
+ * w_scale[n, g] * acc_g[m, n, g], in fp64 (each product is exact; the sum
+ * runs over g in order), returned unrounded.  cond[m, n] = (s_m / 127) *
+ * sum_g |w_scale[n, g] * acc_g[m, n, g]| bounds what any summation order of
+ * the terms can lose to rounding. */
+void oracle_epilogue_grouped(const int32_t *acc_g, const float *scale, const float *w_scale, int64_t M, int64_t N,
+                             int64_t ng, double *y, double *cond) {
+  for (int64_t m = 0; m < M; m++)
+    for (int64_t n = 0; n < N; n++) {
+      double t = 0.0, c = 0.0;
+      for (int64_t g = 0; g < ng; g++) {
+        double p = (double)acc_g[(m * N + n) * ng + g] * (double)w_scale[n * ng + g];
+        t += p;
+        c += fabs(p);
+      }
+      y[m * N + n] = t * (double)scale[m] / 127.0;
+      cond[m * N + n] = c * (double)scale[m] / 127.0;
+    }
+}

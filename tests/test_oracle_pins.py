@@ -374,3 +374,102 @@ def test_bitlinear_swiglu_matches_two_bitlinears(oracle_mod):
     # the fp32 BitLinear outputs are within one rounding of the exact ones
     ref = np.array([[oracle_mod.silu(float(a)) * float(b) for a, b in zip(ra, rb)] for ra, rb in zip(yg, yu)])
     assert np.allclose(out, ref, rtol=1e-5, atol=1e-12)
+
+
+# ------------------------------------------------- group-wise weight scales --
+
+def test_grouped_worked_example(oracle_mod):
+    g = load_golden("grouped_worked.json")
+    W = np.array(g["W"], dtype=np.float32)
+    packed, ws, am = oracle_mod.pack_weights_grouped(W, g["G"])
+    assert packed.tolist() == g["packed"]
+    assert oracle_mod.unpack_codes(packed, W.size).reshape(W.shape).tolist() == g["ternary"]
+    assert ws.tolist() == g["w_scale"]
+    assert am.tolist() == g["absmean"]
+    acc_g = oracle_mod.contract_grouped(np.array(g["x_q"], dtype=np.int8), packed, W.shape[0], W.shape[1], g["G"])
+    assert acc_g.tolist() == g["acc_g"]
+    y, cond = oracle_mod.epilogue_grouped(acc_g, np.array(g["scale"], dtype=np.float32), ws)
+    assert y.tolist() == g["y"] and cond.tolist() == g["cond"]
+
+
+def test_grouped_groups_are_independent(oracle_mod):
+    """Scaling one group's weights by a power of two leaves every code and
+    beta unchanged and scales that group's absmean exactly (a global or
+    per-row mean would move the thresholds of the other groups)."""
+    rng = np.random.default_rng(11)
+    N, K, G = 6, 512, 128
+    W = rng.standard_normal((N, K)).astype(np.float32) * np.float32(0.02)
+    p0, ws0, am0 = oracle_mod.pack_weights_grouped(W, G)
+    W2 = W.copy()
+    W2[2, G:2 * G] *= np.float32(64.0)
+    W2[5, 3 * G:] *= np.float32(0.125)
+    p1, ws1, am1 = oracle_mod.pack_weights_grouped(W2, G)
+    assert np.array_equal(p0, p1) and np.array_equal(ws0, ws1)
+    expect = am0.copy()
+    expect[2, 1] *= np.float32(64.0)
+    expect[5, 3] *= np.float32(0.125)
+    assert np.array_equal(am1, expect)
+    # and a per-tensor pack of the modified matrix does change codes
+    pt, _, _ = oracle_mod.pack_weights(W2)
+    assert not np.array_equal(pt, p1)
+
+
+def test_grouped_pack_thresholds_per_group(oracle_mod):
+    """Within each group, |w| * gamma_g > 1/2 decides a nonzero code (away
+    from exact ties), with gamma_g = 1 / (mean|W_g| + eps) from that group
+    alone; beta_g counts those codes."""
+    rng = np.random.default_rng(12)
+    N, K, G = 4, 256, 64
+    W = rng.laplace(0.0, 0.01, (N, K)).astype(np.float32)
+    packed, ws, am = oracle_mod.pack_weights_grouped(W, G)
+    q = oracle_mod.unpack_codes(packed, N * K).reshape(N, K)
+    for n in range(N):
+        for gi in range(K // G):
+            w = W[n, gi * G:(gi + 1) * G].astype(np.float64)
+            mean = np.mean(np.abs(w))
+            assert abs(am[n, gi] - mean) <= 1e-6 * mean
+            t = np.abs(w) / mean
+            qq = q[n, gi * G:(gi + 1) * G]
+            clear = np.abs(t - 0.5) > 1e-5
+            assert np.all((qq[clear] != 0) == (t[clear] > 0.5))
+            assert np.all(np.sign(qq) == np.where(qq != 0, np.sign(w), 0))
+            assert ws[n, gi] == np.count_nonzero(qq) / G
+
+
+def test_grouped_one_group_per_row_is_per_channel(oracle_mod):
+    """G = K: each row is ternarised on its own; the bytes of row n equal the
+    per-tensor pack of the 1 x K matrix W[n] (the per-channel scale)."""
+    rng = np.random.default_rng(13)
+    N, K = 5, 96
+    W = (rng.standard_normal((N, K)) * np.exp(rng.standard_normal((N, 1)))).astype(np.float32)
+    packed, ws, am = oracle_mod.pack_weights_grouped(W, K)
+    for n in range(N):
+        p, b, a = oracle_mod.pack_weights(W[n:n + 1])
+        assert np.array_equal(packed[n * K // 4:(n + 1) * K // 4], p)
+        assert ws[n, 0] == np.float32(b) and am[n, 0] == np.float32(a)
+
+
+@pytest.mark.parametrize("M,N,K,G", [(1, 3, 64, 8), (3, 5, 96, 32), (2, 4, 256, 256)])
+def test_grouped_matmul_equals_dense_dequantised_fp64(oracle_mod, M, N, K, G):
+    """Brute force: y = (x_q * s / 127) @ (W_ternary * w_scale[n, k // G])^T
+    with a dense fp64 matmul of the dequantised operands; and the group sums
+    add up to the per-tensor integer product."""
+    rng = np.random.default_rng(M * 100 + N + K)
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    packed = oracle_mod.pack_codes(q)
+    ws = (rng.random((N, K // G)) + 0.1).astype(np.float32)
+    xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    s = (rng.random(M) * 3 + 0.1).astype(np.float32)
+    acc_g = oracle_mod.contract_grouped(xq, packed, N, K, G)
+    assert np.array_equal(acc_g.sum(axis=2), oracle_mod.contract(xq, packed, N, K))
+    y, cond = oracle_mod.epilogue_grouped(acc_g, s, ws)
+    Wd = q.astype(np.float64) * np.repeat(ws.astype(np.float64), G, axis=1)
+    Xd = xq.astype(np.float64) * (s.astype(np.float64)[:, None] / 127.0)
+    y_dense = Xd @ Wd.T
+    assert np.allclose(y, y_dense, rtol=1e-12, atol=1e-12 * np.abs(y_dense).max())
+    assert np.all(cond >= np.abs(y) * (1 - 1e-12))
+    # equal scales reduce to the per-tensor epilogue
+    ws1 = np.full_like(ws, 0.625)
+    y1, _ = oracle_mod.epilogue_grouped(acc_g, s, ws1)
+    acc = oracle_mod.contract(xq, packed, N, K)
+    assert np.allclose(y1, acc * 0.625 * s.astype(np.float64)[:, None] / 127.0, rtol=1e-14, atol=0)
