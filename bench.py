@@ -41,7 +41,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="2b-decode",
-                    choices=["2b-decode", "100b-stream", "gateup-sweep", "prefill-2048", "bitlinear-1024"])
+                    choices=["2b-decode", "100b-stream", "gateup-sweep", "prefill-2048", "bitlinear-1024",
+                             "ffn-2b-decode"])
     ap.add_argument("--layers", type=int, default=30)
     ap.add_argument("--M", type=int, default=None, help="tokens (decode workloads)")
     ap.add_argument("--no-graph", action="store_true")
@@ -49,6 +50,8 @@ def parse():
     ap.add_argument("--unfused", action="store_true",
                     help="decode step as quant_act + w2a8_gemv (two calls) instead of the fused bitlinear call")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--group", type=int, default=0,
+                    help="group-wise weight scales: G consecutive weights of a row per scale (0: one beta per matrix)")
     return ap.parse_args()
 
 
@@ -156,7 +159,10 @@ def build_stack(args, dev, rank):
     stack = []
     for L, rep in layers:
         W = synth.weights_torch(L.N, L.K, L.w_dist, L.w_scale, L.w_seed + 1000 * rep, dev)
-        packed, beta, _ = tw.pack_weights(W)
+        if args.group:
+            packed, beta, _ = tw.pack_weights_grouped(W, args.group)  # beta: [N, K/G] group scales
+        else:
+            packed, beta, _ = tw.pack_weights(W)
         del W
         x = synth.acts_torch(M, L.K, L.x_dist, L.x_seed + 1000 * rep + 7919 * rank, dev, outlier_p=L.outlier_p)
         if not L.x_bf16:
@@ -194,30 +200,43 @@ def run_native(args):
     hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
     if args.workload == "prefill-2048":
         return run_prefill(args, dev, rank, world, bf16_peak, peak_src)
+    if args.workload == "ffn-2b-decode":
+        return run_ffn(args, dev, rank, world, hbm_peak, peak_src)
 
     wl, stack, M = build_stack(args, dev, rank)
     fused = not args.unfused
+    G = args.group
     max_ws = max(max(tw.gemv_workspace_bytes(M, e["L"].N, e["L"].K), tw.bitlinear_workspace_bytes(M, e["L"].N,
                                                                                                  e["L"].K))
                  for e in stack)
     ws = torch.zeros(max_ws, dtype=torch.uint8, device=dev)
-    wbytes = sum(e["L"].N * e["L"].K // 4 for e in stack)
+    # weight bytes streamed per step: packed codes (+ fp32 group scales)
+    wbytes = sum(e["L"].N * e["L"].K // 4 + (4 * e["L"].N * (e["L"].K // G) if G else 0) for e in stack)
     xes = stack[0]["x"].element_size()
     if fused:
-        # fused BitLinear kernel: packed weights + x (bf16/fp32) + w_scale + y
-        gemv_bytes = sum(e["L"].N * e["L"].K // 4 + xes * M * e["L"].K + 4 + 4 * M * e["L"].N for e in stack)
+        # fused BitLinear kernel: weights + x (bf16/fp32) + w_scale + y
+        gemv_bytes = wbytes + sum(xes * M * e["L"].K + (0 if G else 4) + 4 * M * e["L"].N for e in stack)
     else:
-        # GEMV: packed weights + x_q + scales + w_scale + y
-        gemv_bytes = sum(e["L"].N * e["L"].K // 4 + M * e["L"].K + 4 * M + 4 + 4 * M * e["L"].N for e in stack)
+        # GEMV: weights + x_q + scales + w_scale + y
+        gemv_bytes = wbytes + sum(M * e["L"].K + 4 * M + (0 if G else 4) + 4 * M * e["L"].N for e in stack)
+
+    def layer(e, quant):
+        L = e["L"]
+        if fused and G:
+            tw.bitlinear_grouped(e["x"], e["packed"], e["beta"], L.N, L.K, G, out=e["y"], workspace=ws)
+        elif fused:
+            tw.bitlinear(e["x"], e["packed"], e["beta"], L.N, L.K, out=e["y"], workspace=ws)
+        else:
+            if quant:
+                tw.quant_act(e["x"], out=(e["xq"], e["s"]))
+            if G:
+                tw.w2a8_grouped(e["xq"], e["s"], e["packed"], e["beta"], L.N, L.K, G, out=e["y"])
+            else:
+                tw.w2a8_gemv(e["xq"], e["s"], e["packed"], e["beta"], L.N, L.K, out=e["y"], workspace=ws)
 
     def step():
         for e in stack:
-            if fused:
-                tw.bitlinear(e["x"], e["packed"], e["beta"], e["L"].N, e["L"].K, out=e["y"], workspace=ws)
-            else:
-                tw.quant_act(e["x"], out=(e["xq"], e["s"]))
-                tw.w2a8_gemv(e["xq"], e["s"], e["packed"], e["beta"], e["L"].N, e["L"].K, out=e["y"],
-                             workspace=ws)
+            layer(e, True)
 
     tw.set_pdl(not args.no_pdl)
     stream = torch.cuda.Stream(dev)
@@ -254,11 +273,7 @@ def run_native(args):
         gemv_graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gemv_graph, stream=stream):
             for e in stack:
-                if fused:
-                    tw.bitlinear(e["x"], e["packed"], e["beta"], e["L"].N, e["L"].K, out=e["y"], workspace=ws)
-                else:
-                    tw.w2a8_gemv(e["xq"], e["s"], e["packed"], e["beta"], e["L"].N, e["L"].K, out=e["y"],
-                                 workspace=ws)
+                layer(e, False)
         for _ in range(2):
             gemv_graph.replay()
         n_meas = max(3, args.steps)
@@ -282,7 +297,10 @@ def run_native(args):
         def e2e_step():
             for e, xh, yh in zip(stack, hx, hy):
                 xd = xh.to(dev, non_blocking=True)
-                y = tw.bitlinear(xd, e["packed"], e["beta"], e["L"].N, e["L"].K)
+                if G:
+                    y = tw.bitlinear_grouped(xd, e["packed"], e["beta"], e["L"].N, e["L"].K, G)
+                else:
+                    y = tw.bitlinear(xd, e["packed"], e["beta"], e["L"].N, e["L"].K)
                 yh.copy_(y, non_blocking=True)
 
         for _ in range(2):
@@ -305,14 +323,21 @@ def run_native(args):
     achieved = gemv_bytes * n_meas / (gemv_ms * 1e-3) / 1e9
     # kernels per BitLinear: fused M <= 2: 1; fused M >= 3: prep + tensor-core GEMV;
     # unfused: quant_act (+ prep for M >= 3) + GEMV
-    per_layer = (1 if M <= 2 else 2) if fused else (2 if M <= 2 else 3)
-    kname = ("gemv_rows_kernel" if M <= 2 else "gemv_tc_kernel") + (" (fused quant)" if fused else "")
+    if G:
+        # fused M <= 2: one streaming kernel; otherwise quant_act + the generic grouped kernel
+        per_layer = 1 if (fused and M <= 2) else 2
+        kname = ("gemv_ldg_kernel grouped form" if M <= 2 else "grouped_generic_kernel") + \
+            (" (fused quant)" if fused and M <= 2 else "")
+    else:
+        per_layer = (1 if M <= 2 else 2) if fused else (2 if M <= 2 else 3)
+        kname = ("gemv_ldg_kernel" if M <= 2 else "gemv_mma_kernel (+prep)") + (" (fused quant)" if fused else "")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded, weights and activations drawn on device)",
         "config": {"workload": f"{wl.name}: {wl.description}", "layers_in_stack": len(stack), "M": M,
-                   "step": "fused bitlinear per layer" if fused else "quant_act + w2a8_gemv per layer",
+                   "step": ("fused bitlinear" if fused else "quant_act + w2a8_gemv") + " per layer"
+                           + (f" with group-wise scales, G={G} (weight bytes include the fp32 scales)" if G else ""),
                    "packed_weight_bytes_per_step": wbytes, "graph": not args.no_graph, "pdl": not args.no_pdl,
                    "l2": "inputs larger than L2 (packed stack %.0f MB > 126 MB L2)" % (wbytes / 1e6),
                    "parallelism": f"replicas x{world}"},
@@ -323,6 +348,169 @@ def run_native(args):
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": per_layer * len(stack) * args.steps,
         "gemv_only_GBps": round(wbytes * n_meas / (gemv_ms * 1e-3) / 1e9, 2),
+        "clocks": clk,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def graph_of(fn, stream):
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def time_replays(graph, n, stream):
+    import torch
+
+    for _ in range(2):
+        graph.replay()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
+def run_ffn(args, dev, rank, world, hbm_peak, peak_src):
+    """Feed-forward decode: per layer silu(gate(h)) * up(h) from the fused
+    gate+up matrix (one call, one streaming kernel for M <= 2), then the down
+    BitLinear on that product.  Every layer has its own weights and h."""
+    import torch
+    import torch.distributed as dist
+
+    import ternary_weight_05_b300 as tw
+    from ternary_weight_05_b300 import synth
+
+    wl = synth.workload("ffn-2b-decode")
+    gu, dn = wl.layers
+    I, D = gu.N // 2, gu.K
+    M = args.M or 1
+    stack = []
+    for r in range(args.layers):
+        W = synth.weights_torch(gu.N, gu.K, gu.w_dist, gu.w_scale, gu.w_seed + 1000 * r, dev)
+        pgu, bgu, _ = tw.pack_weights(W)
+        W = synth.weights_torch(dn.N, dn.K, dn.w_dist, dn.w_scale, dn.w_seed + 1000 * r, dev)
+        pd, bd, _ = tw.pack_weights(W)
+        del W
+        x = synth.acts_torch(M, D, gu.x_dist, gu.x_seed + 1000 * r + 7919 * rank, dev, outlier_p=gu.outlier_p)
+        stack.append(dict(pg=pgu[:I], pu=pgu[I:], bgu=bgu, pd=pd, bd=bd, x=x,
+                          a=torch.empty((M, I), dtype=torch.float32, device=dev),
+                          y=torch.empty((M, D), dtype=torch.float32, device=dev)))
+    torch.cuda.synchronize(dev)
+    ws = torch.zeros(max(tw.bitlinear_swiglu_workspace_bytes(M, I, D), tw.bitlinear_workspace_bytes(M, D, I)),
+                     dtype=torch.uint8, device=dev)
+    wbytes = args.layers * (gu.N * gu.K // 4 + dn.N * dn.K // 4)
+    xes = stack[0]["x"].element_size()
+    # algorithmic bytes of the gate/up SwiGLU kernel: both matrices, h, two
+    # scales, the product a
+    swiglu_bytes = 2 * I * D // 4 + xes * M * D + 8 + 4 * M * I
+
+    def swiglu_all():
+        for e in stack:
+            tw.bitlinear_swiglu(e["x"], e["pg"], e["bgu"], e["pu"], e["bgu"], I, D, out=e["a"], workspace=ws)
+
+    def down_all():
+        for e in stack:
+            tw.bitlinear(e["a"], e["pd"], e["bd"], D, I, out=e["y"], workspace=ws)
+
+    def step():
+        for e in stack:
+            tw.bitlinear_swiglu(e["x"], e["pg"], e["bgu"], e["pu"], e["bgu"], I, D, out=e["a"], workspace=ws)
+            tw.bitlinear(e["a"], e["pd"], e["bd"], D, I, out=e["y"], workspace=ws)
+
+    tw.set_pdl(not args.no_pdl)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        step()
+        torch.cuda.synchronize(dev)
+        graph = graph_of(step, stream)
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        clocks = ClockSampler(dev.index or 0)
+        clocks.start()
+        time.sleep(0.3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_total = e0.elapsed_time(e1)
+        # the dominant kernel (gate/up SwiGLU) and the down BitLinear, each
+        # alone in a graph over the whole stack, same launch configuration
+        n_meas = max(3, args.steps)
+        sw_ms = time_replays(graph_of(swiglu_all, stream), n_meas, stream)
+        dn_ms = time_replays(graph_of(down_all, stream), n_meas, stream)
+        clk = clocks.stop()
+
+        tw.set_pdl(False)
+        hx = [e["x"].cpu().pin_memory() for e in stack]
+        hy = [torch.empty((M, D), dtype=torch.float32).pin_memory() for _ in stack]
+        h2d = sum(t.numel() * t.element_size() for t in hx)
+        d2h = sum(t.numel() * t.element_size() for t in hy)
+
+        def e2e_step():
+            for e, xh, yh in zip(stack, hx, hy):
+                xd = xh.to(dev, non_blocking=True)
+                a = tw.bitlinear_swiglu(xd, e["pg"], e["bgu"], e["pu"], e["bgu"], I, D)
+                yh.copy_(tw.bitlinear(a, e["pd"], e["bd"], D, I), non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e2e_s = time.perf_counter() - t0
+    tw.check_device_error(stream)
+
+    ms_step = ms_total / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step, e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, e2e_s = t[0].item(), t[1].item()
+    value = world * wbytes / (ms_step * 1e-3) / 1e9
+    achieved = swiglu_bytes * args.layers * n_meas / (sw_ms * 1e-3) / 1e9
+    down_bytes = dn.N * dn.K // 4 + 4 * M * I + 4 + 4 * M * D
+    # kernels per layer: M <= 2: the SwiGLU streaming kernel + the down
+    # streaming kernel; M >= 3: gate (prep + GEMV), up (prep + GEMV),
+    # elementwise product, down (prep + GEMV)
+    per_layer = 2 if M <= 2 else 7
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded, weights and activations drawn on device)",
+        "config": {"workload": f"{wl.name}: {wl.description}", "layers_in_stack": args.layers, "M": M,
+                   "step": "per layer: bitlinear_swiglu (gate+up) then bitlinear (down)",
+                   "packed_weight_bytes_per_step": wbytes, "graph": True, "pdl": not args.no_pdl,
+                   "l2": "inputs larger than L2 (packed stack %.0f MB > 126 MB L2)" % (wbytes / 1e6),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "kernel": "gemv_ldg_kernel SwiGLU form (gate+up, fused quant)" if M <= 2
+                     else "gate/up BitLinears + swiglu_kernel", "peak_source": peak_src,
+                     "launches_timed": args.layers * n_meas,
+                     "avg_launch_us": round(1e3 * sw_ms / (args.layers * n_meas), 3)},
+        "down_kernel": {"achieved": round(down_bytes * args.layers * n_meas / (dn_ms * 1e-3) / 1e9, 1),
+                        "unit": "GB/s", "avg_launch_us": round(1e3 * dn_ms / (args.layers * n_meas), 3)},
+        "e2e": {"value": round(world * wbytes * args.steps / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": per_layer * args.layers * args.steps,
         "clocks": clk,
     }
     if rank == 0:
@@ -456,29 +644,58 @@ def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
 # ------------------------------------------------------------ CPU oracle --
 
 def oracle_sample(args):
-    """Host copies of one layer of the workload for the oracle (bounded sample)."""
+    """One layer of the workload for the oracle (bounded sample): a list of
+    (name, packed weight bytes, callable running the oracle on it)."""
+    import numpy as np
+
     import oracle
     from ternary_weight_05_b300 import synth
 
+    def host_packed(L, rep=0):
+        W = synth.weights_np(L.N, L.K, L.w_dist, L.w_scale, seed=L.w_seed + 1000 * rep)
+        packed, beta, _ = oracle.pack_weights(W)
+        return packed, beta
+
+    if args.workload == "ffn-2b-decode":
+        wl = synth.workload("ffn-2b-decode")
+        gu, dn = wl.layers
+        I, D, M = gu.N // 2, gu.K, args.M or 1
+        pgu, bgu = host_packed(gu)
+        pd, bd = host_packed(dn)
+        _, x = synth.acts_np(M, D, gu.x_dist, seed=gu.x_seed, outlier_p=gu.outlier_p)
+
+        def ffn(threads):
+            h = I * D // 4  # the oracle's packed matrix is flat: gate rows, then up rows
+            a, *_ = oracle.bitlinear_swiglu(x, pgu[:h], bgu, pgu[h:], bgu, I, D, threads=threads)
+            oracle.bitlinear(a.astype(np.float32), pd, bd, D, I, threads=threads)
+
+        return [("gate_up+down", gu.N * gu.K // 4 + dn.N * dn.K // 4, ffn)], M
     wl, layers, M = decode_layers(args)
     n = len(wl.layers) if args.workload == "2b-decode" else 1
     sample = []
+    G = args.group
     for L, rep in layers[:n]:
-        W = synth.weights_np(L.N, L.K, L.w_dist, L.w_scale, seed=L.w_seed + 1000 * rep)
-        packed, beta, _ = oracle.pack_weights(W)
         _, x = synth.acts_np(M, L.K, L.x_dist, seed=L.x_seed + 1000 * rep, outlier_p=L.outlier_p, bf16=L.x_bf16)
-        sample.append((L, packed, beta, x))
+        if G:
+            W = synth.weights_np(L.N, L.K, L.w_dist, L.w_scale, seed=L.w_seed + 1000 * rep)
+            packed, ws, _ = oracle.pack_weights_grouped(W, G)
+            sample.append((L.name, L.N * L.K // 4 + 4 * L.N * (L.K // G),
+                           lambda threads, L=L, p=packed, w=ws, x=x: oracle.bitlinear_grouped(
+                               x, p, w, L.N, L.K, G, threads=threads)))
+            continue
+        packed, beta = host_packed(L, rep)
+        sample.append((L.name, L.N * L.K // 4,
+                       lambda threads, L=L, p=packed, b=beta, x=x: oracle.bitlinear(x, p, b, L.N, L.K,
+                                                                                    threads=threads)))
     return sample, M
 
 
 def time_oracle(sample, seconds, threads):
-    import oracle
-
     done_bytes, t0, passes = 0, time.perf_counter(), 0
     while True:
-        for L, packed, beta, x in sample:
-            oracle.bitlinear(x, packed, beta, L.N, L.K, threads=threads)
-            done_bytes += L.N * L.K // 4
+        for _, nbytes, fn in sample:
+            fn(threads)
+            done_bytes += nbytes
         passes += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -490,7 +707,7 @@ def cpu_baseline(args):
         sample, M = oracle_sample(args)
         cores = os.cpu_count() or 1
         gbs, el, passes = time_oracle(sample, args.cpu_seconds, cores)
-        names = ",".join(L.name for L, *_ in sample)
+        names = ",".join(name for name, *_ in sample)
         return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                 "sample": f"{passes} pass(es) over one layer ({names}; M={M}) in {el:.1f} s, "
                           f"rows split over {cores} threads"}
@@ -511,8 +728,8 @@ def run_reference(args):
         gbs, _, _ = time_oracle(sample, per_step, cores)
         vals.append(gbs)
     value = statistics.median(vals)
-    wbytes = sum(L.N * L.K // 4 for L, *_ in sample)
-    names = ",".join(L.name for L, *_ in sample)
+    wbytes = sum(nbytes for _, nbytes, _ in sample)
+    names = ",".join(name for name, *_ in sample)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * wbytes / (value * 1e9), 3),

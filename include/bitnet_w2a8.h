@@ -170,6 +170,109 @@ int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed,
                      int64_t N, int64_t K, float *y, int8_t *x_q, float *scale, int32_t *acc,
                      void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Workspace bytes bitnet_bitlinear_swiglu needs. */
+size_t bitnet_bitlinear_swiglu_workspace_bytes(int64_t M, int64_t I, int64_t K);
+
+/*
+ * bitnet_bitlinear_swiglu -- the front half of the BitTransformer
+ * feed-forward of [Deep-dive] §3.1, down(silu(gate(h)) * up(h)): two
+ * BitLinears on the same activations and their SwiGLU product
+ *   out[m, i] = silu(y_gate[m, i]) * y_up[m, i],  silu(z) = z / (1 + exp(-z)),
+ * with y_gate, y_up formed exactly as bitnet_bitlinear forms y (x quantised
+ * once) and the product in fp32: yg / (1 + expf(-yg)), then * yu, each
+ * operation rounded to nearest.  The down projection is a plain
+ * bitnet_bitlinear on `out` (BITNET_F32).
+ *
+ * For M <= 2 (K % 64 == 0, 512 <= K <= 8192 for one token, <= 4096 for two)
+ * one kernel streams the rows of both matrices and applies the product in
+ * its epilogue.  Other shapes run the gate BitLinear, the up matrix on the
+ * same int8 activations and an elementwise kernel (same arithmetic, same
+ * bits).  A fused gate+up matrix packed as [2I, K] (gate rows first) is
+ * passed as packed_gate = base, packed_up = base + I * K / 4 with the same
+ * w_scale for both.
+ *
+ *   x          device, [M, K] row-major, BITNET_F32 or BITNET_BF16.
+ *   packed_gate, packed_up: device, [I, K / 4] packed codes each (as
+ *              bitnet_pack_weights writes them).
+ *   w_scale_gate, w_scale_up: device, one float each (beta of each matrix).
+ *   out        device, [M, I] float.
+ *   x_q, scale device, [M, K] int8 and [M] float outs, or NULL.
+ *   acc_gate, acc_up: device, [M, I] int32 outs (the exact integer
+ *              products), or NULL.
+ *   workspace  device, >= bitnet_bitlinear_swiglu_workspace_bytes(M, I, K)
+ *              bytes, 256-byte aligned, any contents.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA.
+ */
+int bitnet_bitlinear_swiglu(const void *x, int dtype, int64_t M, const uint8_t *packed_gate,
+                            const float *w_scale_gate, const uint8_t *packed_up,
+                            const float *w_scale_up, int64_t I, int64_t K, float *out, int8_t *x_q,
+                            float *scale, int32_t *acc_gate, int32_t *acc_up, void *workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Group-wise and per-channel weight scales ([Deep-dive] §4.3: in practice the
+ * weights are cut into groups of group_size -- commonly 128 -- and every group
+ * computes its own gamma and beta; one group per output row is the
+ * per-channel scale of [Hands-on] §2.1).  A group is G consecutive weights of
+ * one output row, W[n, g*G .. g*G + G - 1]; a row holds K / G groups.
+ *
+ * bitnet_pack_weights_grouped -- ternarises every group as bitnet_pack_weights
+ * ternarises a whole matrix (mean|W_g| in fp64 over 4096-element chunks left
+ * to right, gamma_g = 1 / (alpha * mean + eps) in fp32, codes
+ * clamp(rint(gamma_g * w), -1, 1) + 1, beta_g = nnz_g / G).
+ *   W        device, [N, K] row-major, BITNET_F32 or BITNET_BF16.
+ *   G        group size: G % 4 == 0, K % G == 0 (G = K: per channel).
+ *   packed   device, N * K / 4 bytes out, the same layout as bitnet_pack_weights.
+ *   w_scale  device, [N, K / G] float out: beta per group.
+ *   absmean  device, [N, K / G] float out (mean|W_g|), or NULL.
+ * No workspace.  Errors: INVALID_ARG, SHAPE, ALIGNMENT, CUDA.
+ */
+int bitnet_pack_weights_grouped(const void *W, int dtype, int64_t N, int64_t K, int64_t G, float alpha,
+                                float eps, uint8_t *packed, float *w_scale, float *absmean,
+                                cudaStream_t stream);
+
+/*
+ * bitnet_w2a8_grouped -- the ternary matmul with group scales, any M:
+ *   y[m, n] = fl(F * fl(s_m / 127)),  F = sum_g acc_g[m, n] * w_scale[n, g]
+ * where acc_g is the exact int32 product of group g (sum over its K range of
+ * (code - 1) * x_q) and F is formed in fp32 (one rounding per group term and
+ * per addition; the order is the kernel's).  The relative error of y against
+ * the exact value is at most about (K / G + 3) * 2^-24 of
+ * (s_m / 127) * sum_g |acc_g * w_scale[n, g]|.
+ * One or two tokens (K % 64 == 0, K <= 8192 / 4096, G = K or a power of two
+ * from 64 to 2048, x_q and packed 16-byte aligned) stream through one kernel
+ * at HBM speed; other shapes use a plain one-warp-per-output kernel.
+ *   x_q, scale, packed: as bitnet_w2a8_gemv.
+ *   w_scale  device, [N, K / G] float (any values, e.g. beta or mean|W_g|).
+ *   y        device, [M, N] float out.
+ *   acc_g    device, [M, N, K / G] int32 out (per-group products), or NULL.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, CUDA.
+ */
+int bitnet_w2a8_grouped(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
+                        const float *w_scale, int64_t N, int64_t K, int64_t G, float *y,
+                        int32_t *acc_g, cudaStream_t stream);
+
+/* Workspace bytes bitnet_bitlinear_grouped needs (its unfused fallback's
+ * int8 activations and scales). */
+size_t bitnet_bitlinear_grouped_workspace_bytes(int64_t M, int64_t K);
+
+/*
+ * bitnet_bitlinear_grouped -- the BitLinear forward with group scales:
+ * per-token absmax quantisation of x (bitnet_quant_act's arithmetic), then
+ * bitnet_w2a8_grouped.  For one or two tokens on the streaming kernel's
+ * shapes the quantisation runs in that kernel's prologue (one kernel).
+ *   x        device, [M, K], BITNET_F32 or BITNET_BF16.
+ *   x_q, scale: device outs ([M, K] int8, [M] float), or NULL.
+ *   workspace device, >= bitnet_bitlinear_grouped_workspace_bytes(M, K),
+ *            256-byte aligned, any contents.
+ *   other arguments as bitnet_w2a8_grouped.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE, CUDA.
+ */
+int bitnet_bitlinear_grouped(const void *x, int dtype, int64_t M, const uint8_t *packed,
+                             const float *w_scale, int64_t N, int64_t K, int64_t G, float *y,
+                             int8_t *x_q, float *scale, int32_t *acc_g, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
 /* Bytes of the fixed device array behind bitnet_w2a8_gemv_static_scratch. */
 #define BITNET_GEMV_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
 

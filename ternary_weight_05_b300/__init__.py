@@ -219,3 +219,118 @@ def bitlinear(x: torch.Tensor, packed: torch.Tensor, w_scale: torch.Tensor, N: i
     if want_xq:
         res += (xq, sc)
     return res[0] if len(res) == 1 else res
+
+
+def bitlinear_swiglu_workspace_bytes(M: int, I: int, K: int) -> int:
+    return int(_L().bitnet_bitlinear_swiglu_workspace_bytes(M, I, K))
+
+
+def bitlinear_swiglu(x: torch.Tensor, packed_gate: torch.Tensor, w_scale_gate: torch.Tensor,
+                     packed_up: torch.Tensor, w_scale_up: torch.Tensor, I: int, K: int, want_acc: bool = False,
+                     want_xq: bool = False, out=None, workspace=None):
+    """Front half of the BitLinear feed-forward: silu(gate(x)) * up(x), fp32 [M, I].
+
+    packed_gate / packed_up are [I, K/4] uint8 (two views of one [2I, K/4]
+    fused gate+up matrix work too); with want_acc also the exact int32
+    products (acc_gate, acc_up), with want_xq the int8 activations and scales.
+    """
+    for t, nm in ((x, "x"), (packed_gate, "packed_gate"), (w_scale_gate, "w_scale_gate"),
+                  (packed_up, "packed_up"), (w_scale_up, "w_scale_up")):
+        _dev(t, nm)
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    M = x.shape[0]
+    dev = x.device
+    a = out if out is not None else torch.empty((M, I), dtype=torch.float32, device=dev)
+    acc_g = torch.empty((M, I), dtype=torch.int32, device=dev) if want_acc else None
+    acc_u = torch.empty((M, I), dtype=torch.int32, device=dev) if want_acc else None
+    xq = torch.empty((M, K), dtype=torch.int8, device=dev) if want_xq else None
+    sc = torch.empty(M, dtype=torch.float32, device=dev) if want_xq else None
+    nbytes = bitlinear_swiglu_workspace_bytes(M, I, K)
+    stream = _stream(dev)
+    if workspace is None:
+        workspace = _ws.get(dev, "bitlinear_swiglu", nbytes, stream)
+    ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+    st = _L().bitnet_bitlinear_swiglu(x.data_ptr(), _dtype_code(x), M, packed_gate.data_ptr(),
+                                      w_scale_gate.data_ptr(), packed_up.data_ptr(), w_scale_up.data_ptr(), I, K,
+                                      a.data_ptr(), ptr(xq), ptr(sc), ptr(acc_g), ptr(acc_u), workspace.data_ptr(),
+                                      workspace.numel(), stream)
+    _lib.check("bitnet_bitlinear_swiglu", st)
+    res = (a,)
+    if want_acc:
+        res += (acc_g, acc_u)
+    if want_xq:
+        res += (xq, sc)
+    return res[0] if len(res) == 1 else res
+
+
+def pack_weights_grouped(W: torch.Tensor, G: int, alpha: float = 1.0, eps: float = 1e-8):
+    """Group-wise absmean ternarisation of W [N, K] (fp32 / bf16, on the GPU):
+    every G consecutive weights of a row form a group with its own gamma and
+    beta (G = K: per output channel).
+
+    Returns (packed uint8 [N, K//4], w_scale float32 [N, K//G] (beta per
+    group), absmean float32 [N, K//G])."""
+    _dev(W, "W")
+    if W.dim() != 2:
+        raise ValueError("W must be 2-D [N, K]")
+    N, K = W.shape
+    dev = W.device
+    packed = torch.empty((N, K // 4), dtype=torch.uint8, device=dev)
+    ng = K // G if G > 0 else 0
+    w_scale = torch.empty((N, ng), dtype=torch.float32, device=dev)
+    absmean = torch.empty((N, ng), dtype=torch.float32, device=dev)
+    st = _L().bitnet_pack_weights_grouped(W.data_ptr(), _dtype_code(W), N, K, G, alpha, eps, packed.data_ptr(),
+                                          w_scale.data_ptr(), absmean.data_ptr(), _stream(dev))
+    _lib.check("bitnet_pack_weights_grouped", st)
+    return packed, w_scale, absmean
+
+
+def w2a8_grouped(x_q, scale, packed, w_scale, N: int, K: int, G: int, want_acc: bool = False, out=None):
+    """Ternary matmul with group scales w_scale [N, K//G], any M: y fp32 [M, N]
+    (and the exact per-group int32 products [M, N, K//G] if asked)."""
+    for t, nm in ((x_q, "x_q"), (scale, "scale"), (packed, "packed"), (w_scale, "w_scale")):
+        _dev(t, nm)
+    M = x_q.shape[0]
+    dev = x_q.device
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=dev)
+    acc = torch.empty((M, N, K // G), dtype=torch.int32, device=dev) if want_acc else None
+    st = _L().bitnet_w2a8_grouped(x_q.data_ptr(), scale.data_ptr(), M, packed.data_ptr(), w_scale.data_ptr(), N, K,
+                                  G, y.data_ptr(), acc.data_ptr() if acc is not None else None, _stream(dev))
+    _lib.check("bitnet_w2a8_grouped", st)
+    return (y, acc) if want_acc else y
+
+
+def bitlinear_grouped(x: torch.Tensor, packed: torch.Tensor, w_scale: torch.Tensor, N: int, K: int, G: int,
+                      want_acc: bool = False, want_xq: bool = False, out=None, workspace=None):
+    """BitLinear forward with group scales: x [M, K] bf16/fp32 -> y fp32 [M, N];
+    with want_acc also the per-group products, with want_xq (x_q, scale)."""
+    for t, nm in ((x, "x"), (packed, "packed"), (w_scale, "w_scale")):
+        _dev(t, nm)
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    M = x.shape[0]
+    dev = x.device
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=dev)
+    acc = torch.empty((M, N, K // G), dtype=torch.int32, device=dev) if want_acc else None
+    xq = torch.empty((M, K), dtype=torch.int8, device=dev) if want_xq else None
+    sc = torch.empty(M, dtype=torch.float32, device=dev) if want_xq else None
+    nbytes = bitlinear_grouped_workspace_bytes(M, K)
+    stream = _stream(dev)
+    if workspace is None:
+        workspace = _ws.get(dev, "bitlinear_grouped", nbytes, stream)
+    ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+    st = _L().bitnet_bitlinear_grouped(x.data_ptr(), _dtype_code(x), M, packed.data_ptr(), w_scale.data_ptr(), N, K,
+                                       G, y.data_ptr(), ptr(xq), ptr(sc), ptr(acc), workspace.data_ptr(),
+                                       workspace.numel(), stream)
+    _lib.check("bitnet_bitlinear_grouped", st)
+    res = (y,)
+    if want_acc:
+        res += (acc,)
+    if want_xq:
+        res += (xq, sc)
+    return res[0] if len(res) == 1 else res
+
+
+def bitlinear_grouped_workspace_bytes(M: int, K: int) -> int:
+    return int(_L().bitnet_bitlinear_grouped_workspace_bytes(M, K))

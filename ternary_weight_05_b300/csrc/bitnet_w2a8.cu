@@ -15,9 +15,9 @@
 #include "gemm.cuh"
 #include "gemv.cuh"
 #include "gemv_ldg.cuh"
-#include "gemv_tc.cuh"
 #include "gemv_mma.cuh"
 #include "gemv_rows.cuh"
+#include "grouped.cuh"
 #include "pack.cuh"
 #include "quant_act.cuh"
 
@@ -129,7 +129,10 @@ struct GemvPlan {
 
 // Token rows of the prepared activations of the mma.sync GEMV (3..16
 // tokens: padded to 8 or 16, K-block-major); 0 for the other kernels.
-int gemv_mma_rows(int64_t M) { return (M >= 3 && M <= 16) ? (M <= 8 ? 8 : 16) : 0; }
+int gemv_mma_rows(int64_t M) {
+  if (M < 3 || M > BITNET_GEMV_MAX_M) return 0;
+  return M <= 8 ? 8 : (M <= 16 ? 16 : (M <= 32 ? 32 : 64));
+}
 
 GemvPlan plan_gemv(int64_t M, int64_t N, int64_t K, int sms) {
   GemvPlan pl = {};
@@ -202,14 +205,35 @@ unsigned prep_grid(int64_t M, const GemvPlan &pl) {
 // fit in registers: 16-byte chunks per row <= 32 lanes x 4 (one token) or x 2.
 int ldg_chunks_per_lane(int64_t M, int64_t K) { return (int)cdiv(K / 64, 32) * (M == 1 ? 1 : 2); }
 bool ldg_ok(int64_t M, int64_t K, const void *packed) {
-  return M <= 2 && K % 64 == 0 && aligned(packed, 16) && ldg_chunks_per_lane(M, K) <= 4;
+  return M <= 2 && K % 64 == 0 && aligned(packed, 16) && ldg_chunks_per_lane(M, K) <= 4 &&
+         M * (K / 16) <= (int64_t)kLdgGroups * kLdgThreads && K / 4 <= kLdgStageBytes;
 }
 
-template <typename XT>
+// Group sizes the streaming kernel takes: one group per row, or a power of
+// two from 64 to 2048 weights (whole runs of 1..32 lanes).
+bool ldg_group_ok(int64_t K, int64_t G) {
+  return G == K || (G >= 64 && G <= 2048 && (G & (G - 1)) == 0 && K % G == 0);
+}
+
+// FORM kLdgSwiGLU: `packed`, `w_scale`, `acc` are the gate matrix's and
+// packed_up, w_scale_up, acc_up the up matrix's (N rows each), y = silu(gate) * up.
+// FORM kLdgGrouped: w_scale is [N, K / G] group scales, acc [M, N, K / G].
+template <typename XT, int FORM = kLdgPlain>
 bitnet_status launch_gemv_ldg(const int8_t *x_q, const float *scale, const void *x, int8_t *xq_out, float *scale_out,
                               int64_t M, const uint8_t *packed, const float *w_scale, int64_t N, int64_t K, float *y,
-                              int32_t *acc, const DeviceInfo *d, cudaStream_t stream) {
+                              int32_t *acc, const DeviceInfo *d, cudaStream_t stream,
+                              const uint8_t *packed_up = nullptr, const float *w_scale_up = nullptr,
+                              int32_t *acc_up = nullptr, int64_t G = 0) {
+  constexpr bool SW = FORM == kLdgSwiGLU, GR = FORM == kLdgGrouped;
   GemvLdgParams p = {};
+  if (GR) {
+    p.G = (int)G;
+    p.NG = (int)(K / G);
+    p.P = (int)(G / 64);
+  }
+  p.packed_up = packed_up;
+  p.w_scale_up = w_scale_up;
+  p.acc_up = acc_up;
   p.packed = packed;
   p.xq = x_q;
   p.x = x;
@@ -223,23 +247,32 @@ bitnet_status launch_gemv_ldg(const int8_t *x_q, const float *scale, const void 
   p.K = K;
   p.M = (int)M;
   p.C = (int)(K / 64);
-  p.SR = (int)std::max<int64_t>(1, kLdgStageBytes / (K / 4));
+#ifndef BITNET_LDG_GRID_MULT
+#define BITNET_LDG_GRID_MULT 1
+#endif
+  const int grid = (int)std::min<int64_t>((int64_t)d->sms * BITNET_LDG_GRID_MULT, cdiv(N, kLdgWarps));
+  // ring sized to the rows a warp owns: at most ceil(N / warps) rows
+  // (SwiGLU: gate and up rows; grouped: the packed row and its scales)
+  const int64_t rowb = (SW ? 2 : 1) * (K / 4) + (GR ? 4 * (K / G) : 0);
+  const int64_t rpw = cdiv(N, (int64_t)grid * kLdgWarps);
+  p.SR = (int)std::max<int64_t>(1, std::min<int64_t>(kLdgStageBytes / rowb, rpw));
+  p.RS = (int)((p.SR * rowb + 15) & ~(int64_t)15);
+  p.NS = (int)std::min<int64_t>(kLdgStages, cdiv(rpw, p.SR));
   const int J = (int)cdiv(p.C, 32);
-  const size_t smem = gemv_ldg_smem_layout((int)M, p.C).bytes + 128;
-  const int grid = (int)std::min<int64_t>(d->sms, cdiv(N, kLdgWarps));
+  const size_t smem = gemv_ldg_smem_layout((int)M, p.C, p.RS, p.NS, GR ? p.NG : 0).bytes + 128;
   auto run = [&](auto kernel) -> bitnet_status {
     if (set_smem(kernel, smem) != BITNET_OK) return BITNET_ERR_CUDA;
     return launch(kernel, dim3(grid), dim3(kLdgThreads), smem, stream, p);
   };
   if (M == 1) {
     switch (J) {
-      case 1: return run(gemv_ldg_kernel<1, 1, XT>);
-      case 2: return run(gemv_ldg_kernel<1, 2, XT>);
-      case 3: return run(gemv_ldg_kernel<1, 3, XT>);
-      default: return run(gemv_ldg_kernel<1, 4, XT>);
+      case 1: return run(gemv_ldg_kernel<1, 1, XT, FORM>);
+      case 2: return run(gemv_ldg_kernel<1, 2, XT, FORM>);
+      case 3: return run(gemv_ldg_kernel<1, 3, XT, FORM>);
+      default: return run(gemv_ldg_kernel<1, 4, XT, FORM>);
     }
   }
-  return J == 1 ? run(gemv_ldg_kernel<2, 1, XT>) : run(gemv_ldg_kernel<2, 2, XT>);
+  return J == 1 ? run(gemv_ldg_kernel<2, 1, XT, FORM>) : run(gemv_ldg_kernel<2, 2, XT, FORM>);
 }
 
 // The row-range kernel takes one or two tokens whose activation words fit in
@@ -286,49 +319,39 @@ bitnet_status launch_gemv_rows(const int8_t *x_q, const float *scale, const void
   return launch(k, dim3(grid), dim3(kRowsThreads), smem, stream, m64, m8, r);
 }
 
-// Decode GEMV on the tensor cores (3 <= M <= 64): activation prep, then the
-// stream-K tcgen05 kernel with NT = 16, 32 or 64 token columns.
+// Decode GEMV on the tensor path (3 <= M <= 64): activation prep (fp16,
+// K-block-major, 8/16/32/64 token rows), then the stream-K mma.sync kernel.
 // With x_q == nullptr the prepared activations are already in the workspace
 // (the fused BitLinear prologue wrote them).
-bitnet_status launch_gemv_tc(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
-                             const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc, void *workspace,
-                             const GemvPlan &pl, const DeviceInfo *d, cudaStream_t stream) {
+bitnet_status launch_gemv_mma(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
+                              const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc, void *workspace,
+                              const GemvPlan &pl, const DeviceInfo *d, cudaStream_t stream) {
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   uint32_t *xb = reinterpret_cast<uint32_t *>(ws + pl.ws_prep_xb);
   int32_t *xsum = reinterpret_cast<int32_t *>(ws + pl.ws_prep_sums);
   float *fscale = reinterpret_cast<float *>(ws + pl.ws_prep_sums + (size_t)M * 4);
-  // 3..16 tokens: mma.sync kernel (8 or 16 token rows, K-block-major
-  // activations: one box per unit); 17..64: tcgen05 kernel
-  const bool mma = M <= 16;
-  const int NT = mma ? gemv_mma_rows(M) : (M <= 32 ? 32 : 64);
+  const int NT = gemv_mma_rows(M);
   if (x_q) {
     bitnet_status st = launch(gemm_prep_kernel, dim3(prep_grid(M, pl)), dim3(256), 0, stream, x_q, scale, w_scale,
                               K, xb, xsum, fscale, M, static_cast<uint4 *>(workspace), (int64_t)(pl.ws_zero_bytes / 16),
-                              mma ? NT : 0);
+                              NT);
     if (st) return st;
   }
   CUtensorMap wmap, bmap;
-  if (bitnet_status s = encode_packed_map(&wmap, packed, N, K, 128, kTcRows, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
-  if (mma) {
-    cuuint64_t dims[2] = {(cuuint64_t)kTcKB, (cuuint64_t)(K / kTcKB) * (cuuint64_t)NT};
-    cuuint64_t strides[1] = {(cuuint64_t)kTcKB * 2};
-    cuuint32_t box[2] = {kTcKB, (cuuint32_t)(8 * NT)};
-    cuuint32_t estr[2] = {1, 1};
-    if (g_encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xb, dims, strides, box, estr,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return BITNET_ERR_CUDA;
-  } else {
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {kTcKB, (cuuint32_t)NT};
+  if (bitnet_status s = encode_packed_map(&wmap, packed, N, K, 128, kMmaRows, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
+  {
+    // the activation slice of a unit: 8 K-blocks x NT token rows of 128 bytes,
+    // one box (two for 64 tokens: a box is at most 256 rows)
+    cuuint64_t dims[2] = {(cuuint64_t)kMmaKB, (cuuint64_t)(K / kMmaKB) * (cuuint64_t)NT};
+    cuuint64_t strides[1] = {(cuuint64_t)kMmaKB * 2};
+    cuuint32_t box[2] = {kMmaKB, (cuuint32_t)std::min(8 * NT, 256)};
     cuuint32_t estr[2] = {1, 1};
     if (g_encode(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xb, dims, strides, box, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return BITNET_ERR_CUDA;
   }
-  GemvTcParams p = {};
+  GemvMmaParams p = {};
   p.y = y;
   p.acc = acc;
   p.xsum = xsum;
@@ -338,27 +361,21 @@ bitnet_status launch_gemv_tc(const int8_t *x_q, const float *scale, int64_t M, c
   p.N = N;
   p.K = K;
   p.M = (int)M;
-  p.NRT = (int)cdiv(N, kTcRows);
-  p.NCH = (int)cdiv(K, kTcChunkK);
-  p.NKB = (int)(K / kTcKB);
+  p.NRT = (int)cdiv(N, kMmaRows);
+  p.NCH = (int)cdiv(K, kMmaChunkK);
+  p.NKB = (int)(K / kMmaKB);
   p.units = (long long)p.NRT * p.NCH;
-  if (mma) {
-    const int grid = (int)std::min<long long>(d->sms, p.units);
-    auto runm = [&](auto kernel, size_t smem) -> bitnet_status {
-      if (set_smem(kernel, smem) != BITNET_OK) return BITNET_ERR_CUDA;
-      return launch(kernel, dim3(grid), dim3(kMmaThreads), smem, stream, wmap, bmap, p);
-    };
-    return NT == 8 ? runm(gemv_mma_kernel<1>, GemvMmaSmem<1>::bytes + 1024)
-                   : runm(gemv_mma_kernel<2>, GemvMmaSmem<2>::bytes + 1024);
-  }
-  const int grid = (int)std::min<long long>((long long)d->sms * kTcCtasPerSm, p.units);
-  auto run = [&](auto kernel, size_t smem) -> bitnet_status {
+  auto run = [&](auto kernel, size_t smem, int ctas) -> bitnet_status {
     if (set_smem(kernel, smem) != BITNET_OK) return BITNET_ERR_CUDA;
-    return launch(kernel, dim3(grid), dim3(kTcThreads), smem, stream, wmap, bmap, p);
+    const int grid = (int)std::min<long long>((long long)d->sms * ctas, p.units);
+    return launch(kernel, dim3(grid), dim3(kMmaThreads), smem, stream, wmap, bmap, p);
   };
-  if (NT == 16) return run(gemv_tc_kernel<16>, GemvTcSmem<16>::bytes + 1024);
-  if (NT == 32) return run(gemv_tc_kernel<32>, GemvTcSmem<32>::bytes + 1024);
-  return run(gemv_tc_kernel<64>, GemvTcSmem<64>::bytes + 1024);
+  switch (NT) {
+    case 8: return run(gemv_mma_kernel<1>, GemvMmaSmem<1>::bytes + 1024, MmaCfg<1>::ctas);
+    case 16: return run(gemv_mma_kernel<2>, GemvMmaSmem<2>::bytes + 1024, MmaCfg<2>::ctas);
+    case 32: return run(gemv_mma_kernel<4>, GemvMmaSmem<4>::bytes + 1024, MmaCfg<4>::ctas);
+    default: return run(gemv_mma_kernel<8>, GemvMmaSmem<8>::bytes + 1024, MmaCfg<8>::ctas);
+  }
 }
 
 bitnet_status check_gemm_args(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
@@ -529,7 +546,7 @@ int bitnet_w2a8_gemv(const int8_t *x_q, const float *scale, int64_t M, const uin
     return launch_gemv_rows<int8_t>(x_q, scale, nullptr, nullptr, nullptr, M, packed, w_scale, N, K, y, acc, d,
                                     stream);
   if (M >= 3 && K <= kTensorMaxK && aligned(x_q, 16))
-    return launch_gemv_tc(x_q, scale, M, packed, w_scale, N, K, y, acc, workspace, pl, d, stream);
+    return launch_gemv_mma(x_q, scale, M, packed, w_scale, N, K, y, acc, workspace, pl, d, stream);
   CUtensorMap map;
   if (bitnet_status s = encode_packed_map(&map, packed, N, K, kStageRowBytes, kStageRows,
                                           CU_TENSOR_MAP_SWIZZLE_128B))
@@ -719,7 +736,7 @@ int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed,
                     xb, xsum, fscale, x_q, scale, M, zero, zero_n16, trows);
     if (st) return st;
     if (M <= BITNET_GEMV_MAX_M)
-      return launch_gemv_tc(nullptr, nullptr, M, packed, w_scale, N, K, y, acc, workspace, pl, d, stream);
+      return launch_gemv_mma(nullptr, nullptr, M, packed, w_scale, N, K, y, acc, workspace, pl, d, stream);
     return launch_gemm_tc(xb, xsum, fscale, M, packed, N, K, y, acc, d, stream);
   }
   // Unfused: quantise into the caller's buffers or the workspace tail, then
@@ -731,6 +748,146 @@ int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed,
   if (M <= BITNET_GEMV_MAX_M)
     return bitnet_w2a8_gemv(xq_buf, s_buf, M, packed, w_scale, N, K, y, acc, workspace, base, stream);
   return bitnet_w2a8_gemm(xq_buf, s_buf, M, packed, w_scale, N, K, y, acc, workspace, base, stream);
+}
+
+size_t bitnet_bitlinear_swiglu_workspace_bytes(int64_t M, int64_t I, int64_t K) {
+  const size_t base = bitnet_bitlinear_workspace_bytes(M, I, K);
+  if (base == 0) return 0;
+  // + y_gate and y_up for the unfused fallback
+  return base + 2 * (((size_t)M * (size_t)I * 4 + 255) & ~(size_t)255);
+}
+
+int bitnet_bitlinear_swiglu(const void *x, int dtype, int64_t M, const uint8_t *packed_gate,
+                            const float *w_scale_gate, const uint8_t *packed_up, const float *w_scale_up, int64_t I,
+                            int64_t K, float *out, int8_t *x_q, float *scale, int32_t *acc_gate, int32_t *acc_up,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!x || !packed_gate || !w_scale_gate || !packed_up || !w_scale_up || !out) return BITNET_ERR_INVALID_ARG;
+  if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_ERR_INVALID_ARG;
+  if (M <= 0 || !shape_ok(I, K) || M > kMaxElems / K || M > kMaxElems / I) return BITNET_ERR_SHAPE;
+  if (I > 0x7fffffff || K > 0x7fffffff || M > 0x7fffffff) return BITNET_ERR_SHAPE;
+  const size_t esz = dtype == BITNET_F32 ? 4 : 2;
+  if (!aligned(x, esz) || !aligned(w_scale_gate, 4) || !aligned(w_scale_up, 4) || !aligned(out, 4) ||
+      !aligned(scale, 4) || !aligned(acc_gate, 4) || !aligned(acc_up, 4))
+    return BITNET_ERR_ALIGNMENT;
+  const size_t need = bitnet_bitlinear_swiglu_workspace_bytes(M, I, K);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return BITNET_ERR_WORKSPACE;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
+
+  // One streaming kernel for one or two tokens: both matrices' rows in each
+  // stage, silu(gate) * up in the epilogue.
+  const bool fused = aligned(x, 16) && (K % 64 == 0) && K >= kStageK && aligned(packed_gate, 16) &&
+                     aligned(packed_up, 16) && aligned(x_q, 16);
+  if (fused && ldg_ok(M, K, packed_gate)) {
+    return dtype == BITNET_BF16
+               ? launch_gemv_ldg<__nv_bfloat16, kLdgSwiGLU>(nullptr, nullptr, x, x_q, scale, M, packed_gate, w_scale_gate,
+                                                      I, K, out, acc_gate, d, stream, packed_up, w_scale_up, acc_up)
+               : launch_gemv_ldg<float, kLdgSwiGLU>(nullptr, nullptr, x, x_q, scale, M, packed_gate, w_scale_gate, I, K,
+                                              out, acc_gate, d, stream, packed_up, w_scale_up, acc_up);
+  }
+  // Otherwise: the gate BitLinear (quantising x), the up matrix on the same
+  // int8 activations, then silu(gate) * up elementwise -- the same fp32
+  // operations as the streaming kernel's epilogue.
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  const size_t base = bitnet_bitlinear_workspace_bytes(M, I, K);
+  const size_t ybytes = ((size_t)M * (size_t)I * 4 + 255) & ~(size_t)255;
+  float *yg = reinterpret_cast<float *>(ws + base);
+  float *yu = reinterpret_cast<float *>(ws + base + ybytes);
+  // the gate call's int8 activations and scales: the caller's buffers or the
+  // tail of the gate call's own workspace (the part the gate call uses only
+  // when it is given no buffers of its own)
+  const size_t mm_ws = M <= BITNET_GEMV_MAX_M ? plan_gemv(M, I, K, d->sms).ws_bytes : gemm_workspace_bytes(M, I, K);
+  int8_t *xq_buf = x_q ? x_q : reinterpret_cast<int8_t *>(ws + mm_ws);
+  float *s_buf = scale ? scale : reinterpret_cast<float *>(ws + mm_ws + (((size_t)M * (size_t)K + 255) & ~(size_t)255));
+  if (int st = bitnet_bitlinear(x, dtype, M, packed_gate, w_scale_gate, I, K, yg, xq_buf, s_buf, acc_gate, workspace,
+                                base, stream))
+    return st;
+  const int st = M <= BITNET_GEMV_MAX_M
+                     ? bitnet_w2a8_gemv(xq_buf, s_buf, M, packed_up, w_scale_up, I, K, yu, acc_up, workspace, mm_ws,
+                                        stream)
+                     : bitnet_w2a8_gemm(xq_buf, s_buf, M, packed_up, w_scale_up, I, K, yu, acc_up, workspace, mm_ws,
+                                        stream);
+  if (st) return st;
+  const int64_t n = M * I;
+  const unsigned grid = (unsigned)std::min<int64_t>((int64_t)d->sms * 8, cdiv(n, 256));
+  return launch(swiglu_kernel, dim3(grid), dim3(256), 0, stream, (const float *)yg, (const float *)yu, out, n);
+}
+
+// ------------------------------------------------- group-wise weight scales --
+
+namespace {
+bool group_shape_ok(int64_t N, int64_t K, int64_t G) {
+  return shape_ok(N, K) && G > 0 && G % 4 == 0 && K % G == 0 && K <= 0x7fffffff && N <= 0x7fffffff;
+}
+}  // namespace
+
+int bitnet_pack_weights_grouped(const void *W, int dtype, int64_t N, int64_t K, int64_t G, float alpha, float eps,
+                                uint8_t *packed, float *w_scale, float *absmean, cudaStream_t stream) {
+  if (!W || !packed || !w_scale) return BITNET_ERR_INVALID_ARG;
+  if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha) || !std::isfinite(eps)) return BITNET_ERR_INVALID_ARG;
+  if (!group_shape_ok(N, K, G)) return BITNET_ERR_SHAPE;
+  if (!aligned(W, dtype == BITNET_F32 ? 4 : 2) || !aligned(w_scale, 4) || !aligned(absmean, 4))
+    return BITNET_ERR_ALIGNMENT;
+  const int64_t groups = N * (K / G);
+  const dim3 grid((unsigned)cdiv(groups, kPackThreads));
+  return dtype == BITNET_F32
+             ? launch(pack_grouped_kernel<float>, grid, dim3(kPackThreads), 0, stream, static_cast<const float *>(W),
+                      groups, G, alpha, eps, packed, w_scale, absmean)
+             : launch(pack_grouped_kernel<__nv_bfloat16>, grid, dim3(kPackThreads), 0, stream,
+                      static_cast<const __nv_bfloat16 *>(W), groups, G, alpha, eps, packed, w_scale, absmean);
+}
+
+int bitnet_w2a8_grouped(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
+                        const float *w_scale, int64_t N, int64_t K, int64_t G, float *y, int32_t *acc_g,
+                        cudaStream_t stream) {
+  if (!x_q || !scale || !packed || !w_scale || !y) return BITNET_ERR_INVALID_ARG;
+  if (M <= 0 || M > 0x7fffffff || !group_shape_ok(N, K, G) || M > kMaxElems / K || M > kMaxElems / N)
+    return BITNET_ERR_SHAPE;
+  if (!aligned(scale, 4) || !aligned(w_scale, 4) || !aligned(y, 4) || !aligned(acc_g, 4))
+    return BITNET_ERR_ALIGNMENT;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
+  if (ldg_ok(M, K, packed) && aligned(x_q, 16) && ldg_group_ok(K, G))
+    return launch_gemv_ldg<int8_t, kLdgGrouped>(x_q, scale, nullptr, nullptr, nullptr, M, packed, w_scale, N, K, y,
+                                                acc_g, d, stream, nullptr, nullptr, nullptr, G);
+  const unsigned grid = (unsigned)std::min<int64_t>((int64_t)d->sms * 16, cdiv(M * N, kGroupedWarps));
+  return launch(grouped_generic_kernel, dim3(grid), dim3(kGroupedWarps * 32), 0, stream, x_q, scale, packed, w_scale,
+                M, N, K, G, y, acc_g);
+}
+
+size_t bitnet_bitlinear_grouped_workspace_bytes(int64_t M, int64_t K) {
+  if (M <= 0 || K <= 0 || M > kMaxElems / K) return 0;
+  return (((size_t)M * (size_t)K + 255) & ~(size_t)255) + (((size_t)M * 4 + 255) & ~(size_t)255);
+}
+
+int bitnet_bitlinear_grouped(const void *x, int dtype, int64_t M, const uint8_t *packed, const float *w_scale,
+                             int64_t N, int64_t K, int64_t G, float *y, int8_t *x_q, float *scale, int32_t *acc_g,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!x || !packed || !w_scale || !y) return BITNET_ERR_INVALID_ARG;
+  if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_ERR_INVALID_ARG;
+  if (M <= 0 || M > 0x7fffffff || !group_shape_ok(N, K, G) || M > kMaxElems / K || M > kMaxElems / N)
+    return BITNET_ERR_SHAPE;
+  const size_t esz = dtype == BITNET_F32 ? 4 : 2;
+  if (!aligned(x, esz) || !aligned(w_scale, 4) || !aligned(y, 4) || !aligned(scale, 4) || !aligned(acc_g, 4))
+    return BITNET_ERR_ALIGNMENT;
+  const size_t need = bitnet_bitlinear_grouped_workspace_bytes(M, K);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return BITNET_ERR_WORKSPACE;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
+  // one streaming kernel (quantisation in its prologue) for one or two tokens
+  if (aligned(x, 16) && aligned(x_q, 16) && ldg_ok(M, K, packed) && ldg_group_ok(K, G)) {
+    return dtype == BITNET_BF16
+               ? launch_gemv_ldg<__nv_bfloat16, kLdgGrouped>(nullptr, nullptr, x, x_q, scale, M, packed, w_scale, N,
+                                                             K, y, acc_g, d, stream, nullptr, nullptr, nullptr, G)
+               : launch_gemv_ldg<float, kLdgGrouped>(nullptr, nullptr, x, x_q, scale, M, packed, w_scale, N, K, y,
+                                                     acc_g, d, stream, nullptr, nullptr, nullptr, G);
+  }
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  int8_t *xq_buf = x_q ? x_q : reinterpret_cast<int8_t *>(ws);
+  float *s_buf = scale ? scale : reinterpret_cast<float *>(ws + (((size_t)M * (size_t)K + 255) & ~(size_t)255));
+  if (int st = bitnet_quant_act(x, dtype, M, K, xq_buf, s_buf, stream)) return st;
+  return bitnet_w2a8_grouped(xq_buf, s_buf, M, packed, w_scale, N, K, G, y, acc_g, stream);
 }
 
 int bitnet_check_device_error(cudaStream_t stream) {

@@ -22,18 +22,51 @@
 //   * Fused form (XT = float / bf16): the CTA quantises x itself in its
 //     prologue (absmax, then clamp(rint(x / s * 127)), the operations of
 //     quant_act_kernel), so one kernel runs the whole BitLinear.
+//   * SwiGLU form (SW): the front half of the BitTransformer feed-forward of
+//     BitNet 深度拆解 §3.1, silu(gate(h)) * up(h).  A stage holds gate rows
+//     and the up rows of the same indices (two bulk copies); both sums are
+//     formed together and lane m writes silu(y_gate) * y_up, each y exactly
+//     as the GEMV epilogue forms it.
+//   * Grouped form (GR): group-wise weight scales (BitNet 深度拆解 §4.3: each
+//     group of G consecutive weights of a row has its own scale; G = K is a
+//     per-channel scale).  A stage also carries its rows' scales (cp.async,
+//     4 bytes each, by all lanes); the per-group Σ x_q come from the
+//     prologue.  With P = G / 64 chunks per group (G <= 2048), aligned runs
+//     of P lanes add their chunk sums by shuffles and the run's first lane
+//     adds (acc_g) * scale_g into an fp32 partial; the warp then adds the
+//     partials and lane m writes F * (s_m / 127).  With one group per row the
+//     row sum is taken whole.
 #pragma once
 
 #include "common.cuh"
 #include "gemv_rows.cuh"
 #include "quant_act.cuh"
+#include "swiglu.cuh"
 
 namespace bitnet {
 
-constexpr int kLdgWarps = 12;
+#ifndef BITNET_LDG_WARPS
+#define BITNET_LDG_WARPS 12
+#endif
+#ifndef BITNET_LDG_MIN_CTAS
+#define BITNET_LDG_MIN_CTAS 1
+#endif
+constexpr int kLdgWarps = BITNET_LDG_WARPS;
 constexpr int kLdgThreads = kLdgWarps * 32;
-constexpr int kLdgStageBytes = 8192;  // per warp stage: whole rows, at most 8 KB
-constexpr int kLdgStages = 2;         // stages per warp
+#ifndef BITNET_LDG_STAGE_BYTES
+#define BITNET_LDG_STAGE_BYTES 8192
+#endif
+// Largest stage and ring per warp; a launch sizes its ring to the rows its
+// warps own (p.RS bytes x p.NS stages), so that small matrices leave room on
+// the SM for the next kernel's CTAs (programmatic dependent launch).
+constexpr int kLdgStageBytes = BITNET_LDG_STAGE_BYTES;  // per warp stage: whole rows
+constexpr int kLdgStages = 16384 / kLdgStageBytes;     // 16 KB of stages per warp
+// Fused prologue: each thread keeps up to kLdgGroups 16-element activation
+// groups in registers between the absmax and the quantisation (one read of
+// x); the host only sends shapes with M * K / 16 <= kLdgGroups * kLdgThreads.
+constexpr int kLdgGroups = 2;
+
+constexpr int kLdgPlain = 0, kLdgSwiGLU = 1, kLdgGrouped = 2;  // kernel forms
 
 struct GemvLdgParams {
   const uint8_t *packed;
@@ -42,14 +75,30 @@ struct GemvLdgParams {
   int8_t *xq_out;     // fused forms, optional (CTA 0)
   float *scale_out;   // fused forms, optional (CTA 0)
   const float *scale;
-  const float *w_scale;
+  const float *w_scale;  // grouped form: [N, NG] group scales
   float *y;
-  int32_t *acc;
-  int64_t N, K;
+  int32_t *acc;          // grouped form: [M, N, NG] per-group products
+  const uint8_t *packed_up;  // SwiGLU form: the up rows (gate rows in `packed`)
+  const float *w_scale_up;
+  int32_t *acc_up;
+  int64_t N, K;  // N: rows (SwiGLU: rows of each of gate and up)
   int M;
   int C;   // 16-byte chunks per packed row (K / 64)
-  int SR;  // rows per stage (SR * K / 4 <= kLdgStageBytes)
+  int SR;  // rows (SwiGLU: row pairs) per stage, SR * K / 4 (x2) <= kLdgStageBytes
+  int RS;  // bytes per stage (SR rows, a multiple of 16)
+  int NS;  // stages per warp (<= kLdgStages)
+  int G, NG, P;  // grouped form: group size, groups per row, 16-byte chunks per group
 };
+
+// 4-byte asynchronous copy global -> shared (per-thread completion groups).
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // 1D bulk copy global -> shared, completing on `bar` (both addresses and the
 // size multiples of 16 bytes), L2 evict-first: the weights are read once.
@@ -64,26 +113,30 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 
 // Shared memory: per-warp stage rings, activation words [MT][C * 64 bytes],
 // per-token sums and output scales, the fused prologue's reduction scratch,
-// then the stage barriers.
+// the stage barriers, then (grouped form) per-group sums [MT][NG].
 struct GemvLdgSmem {
-  int ring, xw, xsum, fscale, redf, bars, bytes;
+  int ring, xw, xsum, fscale, redf, bars, xsumg, bytes;
 };
-__host__ __device__ inline GemvLdgSmem gemv_ldg_smem_layout(int MT, int C) {
+__host__ __device__ inline GemvLdgSmem gemv_ldg_smem_layout(int MT, int C, int RS, int NS, int NG) {
   GemvLdgSmem L;
   L.ring = 0;
-  L.xw = kLdgWarps * kLdgStages * kLdgStageBytes;
+  L.xw = kLdgWarps * NS * RS;
   L.xsum = L.xw + MT * C * 64;
   L.fscale = L.xsum + 32;
   L.redf = L.fscale + 32;
   L.bars = L.redf + kLdgWarps * MT * 4 + 16;
-  L.bytes = L.bars + kLdgWarps * kLdgStages * 8;
+  L.xsumg = L.bars + kLdgWarps * kLdgStages * 8;
+  L.bytes = L.xsumg + MT * NG * 4;
   return L;
 }
 
-template <int MT, int J, typename XT>
-__global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgParams p) {
+template <int MT, int J, typename XT, int FORM>
+__global__ void __launch_bounds__(kLdgThreads, BITNET_LDG_MIN_CTAS) gemv_ldg_kernel(const GemvLdgParams p) {
+  constexpr bool SW = FORM == kLdgSwiGLU, GR = FORM == kLdgGrouped;
   extern __shared__ __align__(128) uint8_t lsm[];
-  const GemvLdgSmem L = gemv_ldg_smem_layout(MT, p.C);
+  const GemvLdgSmem L = gemv_ldg_smem_layout(MT, p.C, p.RS, p.NS, GR ? p.NG : 0);
+  const int NS = p.NS;
+  int32_t *xsumg = reinterpret_cast<int32_t *>(lsm + L.xsumg);  // [MT][NG]
   uint8_t *xw = lsm + L.xw;                                     // [MT][C*64]
   int32_t *xsum = reinterpret_cast<int32_t *>(lsm + L.xsum);    // [MT]
   float *fscale = reinterpret_cast<float *>(lsm + L.fscale);    // [MT]
@@ -96,7 +149,7 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
   const int64_t r0 = (int64_t)(p.N * gw / nw), r1 = (int64_t)(p.N * (gw + 1) / nw);
   const int64_t rowb = p.K / 4;
   const int nst = (int)((r1 - r0 + p.SR - 1) / p.SR);  // this warp's stages
-  uint8_t *ring = lsm + L.ring + (size_t)warp * kLdgStages * kLdgStageBytes;
+  uint8_t *ring = lsm + L.ring + (size_t)warp * NS * p.RS;
   uint64_t *wbar = bars + warp * kLdgStages;
   pdl_launch_dependents();
 
@@ -114,40 +167,67 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
     const int64_t ra = r0 + (int64_t)st * p.SR;
     const int64_t rbn = min(ra + p.SR, r1);
     const uint32_t bytes = (uint32_t)((rbn - ra) * rowb);
-    uint64_t *bar = &wbar[st % kLdgStages];
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_load(ring + (st % kLdgStages) * kLdgStageBytes, p.packed + ra * rowb, bytes, bar, policy);
+    uint64_t *bar = &wbar[st % NS];
+    uint8_t *dst = ring + (st % NS) * p.RS;
+    mbar_arrive_expect_tx(bar, SW ? 2 * bytes : bytes);
+    bulk_load(dst, p.packed + ra * rowb, bytes, bar, policy);
+    if (SW) bulk_load(dst + bytes, p.packed_up + ra * rowb, bytes, bar, policy);
+  };
+  // grouped form: every lane copies part of the stage's scales [rows][NG]
+  // behind its packed rows, and commits one group per stage
+  int issued_s = 0;
+  auto issue_scales = [&](int st) {
+    ++issued_s;
+    const int64_t ra = r0 + (int64_t)st * p.SR;
+    const int nr = (int)(min(ra + p.SR, r1) - ra);
+    float *dst = reinterpret_cast<float *>(ring + (st % NS) * p.RS + (size_t)nr * rowb);
+    const float *src = p.w_scale + ra * p.NG;
+    for (int e = lane; e < nr * p.NG; e += 32) cp_async4(dst + e, src + e);
+    cp_async_commit();
   };
   if (lane == 0) {
     policy = l2_policy_evict_first();
-    for (int st = 0; st < nst && st < kLdgStages; ++st) issue(st);
+    for (int st = 0; st < nst && st < NS; ++st) issue(st);
   }
+  if (GR)
+    for (int st = 0; st < nst && st < NS; ++st) issue_scales(st);
 
   pdl_wait_prior_grid();
   // ---------------------------------------------- activation words (smem) --
   if (tid < MT) xsum[tid] = 0;
+  if (GR)
+    for (int i = tid; i < MT * p.NG; i += kLdgThreads) xsumg[i] = 0;
   if constexpr (std::is_same<XT, int8_t>::value) {
-    if (tid < MT) fscale[tid] = __fdiv_rn(__fmul_rn(__ldg(p.w_scale), __ldg(p.scale + tid)), 127.0f);
+    if (tid < MT) {
+      // grouped form: the token factor s / 127 (the weight scales are per group)
+      fscale[tid] = GR ? __fdiv_rn(__ldg(p.scale + tid), 127.0f)
+                       : __fdiv_rn(__fmul_rn(__ldg(p.w_scale), __ldg(p.scale + tid)), 127.0f);
+      if (SW) fscale[MT + tid] = __fdiv_rn(__fmul_rn(__ldg(p.w_scale_up), __ldg(p.scale + tid)), 127.0f);
+    }
   }
   __syncthreads();
   const int groups = p.C * 4;  // 16-K groups per token
   {
     float s[MT];
+    float f[kLdgGroups][16];  // fused forms: this thread's activation groups
     if constexpr (!std::is_same<XT, int8_t>::value) {
       const XT *x = static_cast<const XT *>(p.x);
       float amax[MT];
 #pragma unroll
       for (int m = 0; m < MT; ++m) amax[m] = 0.0f;
-      for (int i = tid; i < MT * groups; i += kLdgThreads) {
-        const int m = i / groups, q = i % groups;
-        float v[16];
-        rows_load16(x + (int64_t)m * p.K + (int64_t)q * 16, v);
-        float a = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) a = fmaxf(a, fabsf(v[e]));
+      for (int n = 0; n < kLdgGroups; ++n) {
+        const int i = tid + n * kLdgThreads;
+        if (i < MT * groups) {
+          const int m = i / groups, q = i % groups;
+          rows_load16(x + (int64_t)m * p.K + (int64_t)q * 16, f[n]);
+          float a = 0.0f;
 #pragma unroll
-        for (int mm = 0; mm < MT; ++mm)
-          if (mm == m) amax[mm] = fmaxf(amax[mm], a);
+          for (int e = 0; e < 16; ++e) a = fmaxf(a, fabsf(f[n][e]));
+#pragma unroll
+          for (int mm = 0; mm < MT; ++mm)
+            if (mm == m) amax[mm] = fmaxf(amax[mm], a);
+        }
       }
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
@@ -164,38 +244,51 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
         s[m] = a < 1e-8f ? 1e-8f : a;
       }
       if (tid < MT) {
-        fscale[tid] = __fdiv_rn(__fmul_rn(__ldg(p.w_scale), s[tid]), 127.0f);
+        fscale[tid] = GR ? __fdiv_rn(s[tid], 127.0f) : __fdiv_rn(__fmul_rn(__ldg(p.w_scale), s[tid]), 127.0f);
+        if (SW) fscale[MT + tid] = __fdiv_rn(__fmul_rn(__ldg(p.w_scale_up), s[tid]), 127.0f);
         if (blockIdx.x == 0 && p.scale_out) p.scale_out[tid] = s[tid];
       }
     }
     int part[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) part[m] = 0;
-    for (int i = tid; i < MT * groups; i += kLdgThreads) {
-      const int m = i / groups, q = i % groups;
-      int8_t v[16];
-      if constexpr (std::is_same<XT, int8_t>::value) {
+    if constexpr (std::is_same<XT, int8_t>::value) {
+      for (int i = tid; i < MT * groups; i += kLdgThreads) {
+        const int m = i / groups, q = i % groups;
+        int8_t v[16];
         const int4 u = *reinterpret_cast<const int4 *>(p.xq + (int64_t)m * p.K + (int64_t)q * 16);
         memcpy(v, &u, 16);
-      } else {
-        float f[16];
-        rows_load16(static_cast<const XT *>(p.x) + (int64_t)m * p.K + (int64_t)q * 16, f);
-        float sm = s[0];
+        const int sum = rows_pack_group(v, xw + (size_t)m * p.C * 64 + (size_t)q * 16);
+        if (GR && sum) atomicAdd(&xsumg[m * p.NG + (q * 16) / p.G], sum);
 #pragma unroll
-        for (int mm = 1; mm < MT; ++mm)
-          if (mm == m) sm = s[mm];
+        for (int mm = 0; mm < MT; ++mm)
+          if (mm == m) part[mm] += sum;
+      }
+    } else {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = quantize_one(f[e], sm);
-        if (blockIdx.x == 0 && p.xq_out) {
-          int4 u;
-          memcpy(&u, v, 16);
-          *reinterpret_cast<int4 *>(p.xq_out + (int64_t)m * p.K + (int64_t)q * 16) = u;
+      for (int n = 0; n < kLdgGroups; ++n) {
+        const int i = tid + n * kLdgThreads;
+        if (i < MT * groups) {
+          const int m = i / groups, q = i % groups;
+          float sm = s[0];
+#pragma unroll
+          for (int mm = 1; mm < MT; ++mm)
+            if (mm == m) sm = s[mm];
+          int8_t v[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = quantize_one(f[n][e], sm);
+          if (blockIdx.x == 0 && p.xq_out) {
+            int4 u;
+            memcpy(&u, v, 16);
+            *reinterpret_cast<int4 *>(p.xq_out + (int64_t)m * p.K + (int64_t)q * 16) = u;
+          }
+          const int sum = rows_pack_group(v, xw + (size_t)m * p.C * 64 + (size_t)q * 16);
+          if (GR && sum) atomicAdd(&xsumg[m * p.NG + (q * 16) / p.G], sum);
+#pragma unroll
+          for (int mm = 0; mm < MT; ++mm)
+            if (mm == m) part[mm] += sum;
         }
       }
-      const int sum = rows_pack_group(v, xw + (size_t)m * p.C * 64 + (size_t)q * 16);
-#pragma unroll
-      for (int mm = 0; mm < MT; ++mm)
-        if (mm == m) part[mm] += sum;
     }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
@@ -225,75 +318,182 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
       }
     }
   int32_t xs[MT];
-  float fs[MT];
+  float fs[MT], fsu[MT];
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
     xs[m] = xsum[m];
     fs[m] = fscale[m];
+    fsu[m] = SW ? fscale[MT + m] : 0.0f;
   }
 
-  // ------------------------------------------------------------ main loop --
-  bool ok = true;
-  for (int st = 0; st < nst; ++st) {
-    const int slot = st % kLdgStages;
-    if (ok && !mbar_wait(&wbar[slot], (uint32_t)((st / kLdgStages) & 1))) {
-      raise_device_error(kDevErrTimeout);
-      ok = false;  // keep walking (results undefined, the error word says so)
+  // sum over the packed row at `row` (shared memory) of code * x, per token,
+  // combined over the warp: every lane ends with the totals
+  auto row_sums = [&](const uint8_t *row, int (&v)[MT]) {
+    int a[MT][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) a[m][s] = 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int c = lane + 32 * j;
+      uint4 wq = make_uint4(0u, 0u, 0u, 0u);
+      if (c < p.C) wq = lds_u128(smem_u32(row + (size_t)c * 16));
+      const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t f0 = wv[u] & 0x03030303u, f1 = wv[u] & 0x0C0C0C0Cu;
+        const uint32_t f2 = wv[u] & 0x30303030u, f3 = wv[u] & 0xC0C0C0C0u;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          a[m][0] = dp4a_u8s8(f0, xr[m][j][4 * u + 0], a[m][0]);
+          a[m][1] = dp4a_u8s8(f1, xr[m][j][4 * u + 1], a[m][1]);
+          a[m][2] = dp4a_u8s8(f2, xr[m][j][4 * u + 2], a[m][2]);
+          a[m][3] = dp4a_u8s8(f3, xr[m][j][4 * u + 3], a[m][3]);
+        }
+      }
     }
-    const uint8_t *stage = ring + slot * kLdgStageBytes;
-    const int64_t ra = r0 + (int64_t)st * p.SR;
-    const int nr = (int)(min(ra + p.SR, r1) - ra);
-    for (int i = 0; i < nr; ++i) {
-      const int64_t r = ra + i;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      int t = a[m][0] + (a[m][1] >> 2) + (a[m][2] >> 4) + (a[m][3] >> 6);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      v[m] = t;
+    }
+  };
+
+  // grouped form: the fp32 sum over the row's groups of acc_g * scale_g, per
+  // token (every lane ends with the totals).  `sc` holds the row's NG scales;
+  // with `accg` non-null the per-group products go to accg[(m * N + r) * NG + g].
+  auto row_grouped = [&](const uint8_t *row, const float *sc, int64_t r, float (&F)[MT]) {
+    float f[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) f[m] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int c = lane + 32 * j;
+      uint4 wq = make_uint4(0u, 0u, 0u, 0u);
+      if (c < p.C) wq = lds_u128(smem_u32(row + (size_t)c * 16));
+      const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
       int a[MT][4];
 #pragma unroll
       for (int m = 0; m < MT; ++m)
 #pragma unroll
         for (int s = 0; s < 4; ++s) a[m][s] = 0;
 #pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const int c = lane + 32 * j;
-        uint4 wq = make_uint4(0u, 0u, 0u, 0u);
-        if (c < p.C) wq = lds_u128(smem_u32(stage + (size_t)i * rowb + (size_t)c * 16));
-        const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t f0 = wv[u] & 0x03030303u, f1 = wv[u] & 0x0C0C0C0Cu;
+        const uint32_t f2 = wv[u] & 0x30303030u, f3 = wv[u] & 0xC0C0C0C0u;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t f0 = wv[u] & 0x03030303u, f1 = wv[u] & 0x0C0C0C0Cu;
-          const uint32_t f2 = wv[u] & 0x30303030u, f3 = wv[u] & 0xC0C0C0C0u;
-#pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            a[m][0] = dp4a_u8s8(f0, xr[m][j][4 * u + 0], a[m][0]);
-            a[m][1] = dp4a_u8s8(f1, xr[m][j][4 * u + 1], a[m][1]);
-            a[m][2] = dp4a_u8s8(f2, xr[m][j][4 * u + 2], a[m][2]);
-            a[m][3] = dp4a_u8s8(f3, xr[m][j][4 * u + 3], a[m][3]);
-          }
+        for (int m = 0; m < MT; ++m) {
+          a[m][0] = dp4a_u8s8(f0, xr[m][j][4 * u + 0], a[m][0]);
+          a[m][1] = dp4a_u8s8(f1, xr[m][j][4 * u + 1], a[m][1]);
+          a[m][2] = dp4a_u8s8(f2, xr[m][j][4 * u + 2], a[m][2]);
+          a[m][3] = dp4a_u8s8(f3, xr[m][j][4 * u + 3], a[m][3]);
         }
       }
+      // this chunk's sum of code * x, then the run of P lanes of its group
+      const int g = c / p.P;
+      const bool lead = (lane & (p.P - 1)) == 0 && c < p.C;
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
-        int v = a[m][0] + (a[m][1] >> 2) + (a[m][2] >> 4) + (a[m][3] >> 6);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == m) {
-          const int32_t o = v - xs[m];
-          if (p.acc) p.acc[(int64_t)m * p.N + r] = o;
-          p.y[(int64_t)m * p.N + r] = __fmul_rn((float)o, fs[m]);
+        int t = a[m][0] + (a[m][1] >> 2) + (a[m][2] >> 4) + (a[m][3] >> 6);
+        for (int o = 1; o < p.P; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lead) {
+          const int32_t ag = t - xsumg[m * p.NG + g];
+          if (p.acc) p.acc[((int64_t)m * p.N + r) * p.NG + g] = ag;
+          f[m] = __fmaf_rn((float)ag, sc[g], f[m]);
         }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float v = f[m];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+      F[m] = v;
+    }
+  };
+
+  // ------------------------------------------------------------ main loop --
+  bool ok = true;
+  for (int st = 0; st < nst; ++st) {
+    const int slot = st % NS;
+    if (ok && !mbar_wait(&wbar[slot], (uint32_t)((st / NS) & 1))) {
+      raise_device_error(kDevErrTimeout);
+      ok = false;  // keep walking (results undefined, the error word says so)
+    }
+    const uint8_t *stage = ring + slot * p.RS;
+    const int64_t ra = r0 + (int64_t)st * p.SR;
+    const int nr = (int)(min(ra + p.SR, r1) - ra);
+    if (GR) {
+      // this lane's scale copies of the stage are done; then everyone's
+      if (issued_s > st + 1) cp_async_wait<1>();
+      else cp_async_wait<0>();
+      __syncwarp();
+    }
+    for (int i = 0; i < nr; ++i) {
+      const int64_t r = ra + i;
+      if constexpr (GR) {
+        const float *sc = reinterpret_cast<const float *>(stage + (size_t)nr * rowb) + (size_t)i * p.NG;
+        if (p.NG == 1) {
+          // one group per row: the whole-row sum, scaled once
+          int v[MT];
+          row_sums(stage + (size_t)i * rowb, v);
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+            if (lane == m) {
+              const int32_t ag = v[m] - xsumg[m];
+              if (p.acc) p.acc[(int64_t)m * p.N + r] = ag;
+              p.y[(int64_t)m * p.N + r] = __fmul_rn(__fmul_rn((float)ag, sc[0]), fs[m]);
+            }
+        } else {
+          float F[MT];
+          row_grouped(stage + (size_t)i * rowb, sc, r, F);
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+            if (lane == m) p.y[(int64_t)m * p.N + r] = __fmul_rn(F[m], fs[m]);
+        }
+        continue;
+      }
+      int v[MT];
+      row_sums(stage + (size_t)i * rowb, v);
+      if constexpr (SW) {
+        int vu[MT];
+        row_sums(stage + (size_t)(nr + i) * rowb, vu);
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+          if (lane == m) {
+            const int32_t og = v[m] - xs[m], ou = vu[m] - xs[m];
+            if (p.acc) p.acc[(int64_t)m * p.N + r] = og;
+            if (p.acc_up) p.acc_up[(int64_t)m * p.N + r] = ou;
+            p.y[(int64_t)m * p.N + r] = silu_mul(__fmul_rn((float)og, fs[m]), __fmul_rn((float)ou, fsu[m]));
+          }
+      } else {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+          if (lane == m) {
+            const int32_t o = v[m] - xs[m];
+            if (p.acc) p.acc[(int64_t)m * p.N + r] = o;
+            p.y[(int64_t)m * p.N + r] = __fmul_rn((float)o, fs[m]);
+          }
       }
     }
     // every lane's reads of this stage are done: refill it
     __syncwarp();
-    if (lane == 0 && ok && st + kLdgStages < nst) {
+    if (lane == 0 && ok && st + NS < nst) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(st + kLdgStages);
+      issue(st + NS);
     }
+    if (GR && ok && st + NS < nst) issue_scales(st + NS);
   }
   // After a timeout leave no bulk copy in flight (bounded waits on the
   // stages this lane requested last).
   if (!ok && lane == 0) {
-    for (int st = (issued > kLdgStages ? issued - kLdgStages : 0); st < issued; ++st)
-      mbar_wait(&wbar[st % kLdgStages], (uint32_t)((st / kLdgStages) & 1));
+    for (int st = (issued > NS ? issued - NS : 0); st < issued; ++st)
+      mbar_wait(&wbar[st % NS], (uint32_t)((st / NS) & 1));
   }
+  if (GR) cp_async_wait<0>();
 }
 
 }  // namespace bitnet

@@ -1,4 +1,4 @@
-// Decode-path W2A8 ternary GEMV for 3..16 tokens on the mma.sync tensor path.
+// Decode-path W2A8 ternary GEMV for 3..64 tokens on the mma.sync tensor path.
 //
 // Same operation as the other GEMV kernels: y[m, n] = (sum_k (code[n,k]-1) *
 // x_q[m,k]) * (w_scale * s_m / 127), the integer-domain product of BitNet
@@ -6,8 +6,9 @@
 // with the dequantisation of §2.3.
 //
 // A few tokens need 2 * M multiply-adds per weight: more than dp4a sustains
-// at HBM speed for M > 2, while tcgen05 MMAs with N = 8..16 tokens cost far
-// more per instruction than their arithmetic (measured).  mma.sync m16n8k16
+// at HBM speed for M > 2, while tcgen05 MMAs with N = 8..64 tokens cost far
+// more per instruction than their arithmetic (measured: a tcgen05 form of
+// this kernel was slower at every M up to 64).  mma.sync m16n8k16
 // takes A (16 weight rows x 16 K) straight from registers, so decoding costs
 // one AND per two weights and nothing else touches shared memory but the
 // packed weights and the activations:
@@ -20,12 +21,15 @@
 //     contiguous range of units (stream-K).  Each unit's 16 KB of packed
 //     weights and its activation slice (prepared K-block-major, so the slice
 //     is one box) arrive in one stage of a ring with two TMA copies (the cost
-//     of a copy is per box, so boxes are few and large); up to kMmaStages in
+//     of a copy is per box, so boxes are few and large); 3 or 5 stages in
 //     flight, weights requested before waiting on the previous kernel.
-//   * Warp w of the 8 compute warps takes the 64-K column w of every unit for
-//     all 8 row blocks: its activation fragments are loaded once per unit and
-//     reused 8 times.  At the end of a row tile's segment the warps add their
-//     exact int32 partial sums in shared memory; a tile finished inside the
+//   * Up to 16 tokens, warp w of the 8 compute warps takes the 64-K column w
+//     of every unit for all 8 row blocks: its activation fragments are loaded
+//     once per unit and reused 8 times, and the warps' exact int32 partial
+//     sums are added in shared memory.  With 32 or 64 tokens the accumulators
+//     of 8 row blocks would not fit in registers: warp w then takes row block
+//     w over all K-blocks of the unit and owns its outputs alone.  At the end
+//     of a row tile's segment a tile finished inside the
 //     CTA is written directly, a tile split between CTAs is summed with int32
 //     atomics in the workspace and written by the CTA that completes it
 //     (ticket), which re-zeroes the entries.
@@ -34,36 +38,69 @@
 #pragma once
 
 #include "common.cuh"
-#include "gemv_tc.cuh"
 
 namespace bitnet {
 
+constexpr int kMmaRows = 128;    // weight rows per tile
+constexpr int kMmaChunkK = 512;  // K per work unit (one 128-byte column of packed rows)
+constexpr int kMmaKB = 64;       // K per activation block (K-block-major layout)
+
+struct GemvMmaParams {
+  float *y;
+  int32_t *acc;
+  const int32_t *xsum;   // [M] sum of x_q per token
+  const float *fscale;   // [M] w_scale * s_m / 127
+  int32_t *ws_partial;   // [NRT * 128][M], zero on entry and exit
+  unsigned *ws_ticket;   // [NRT], zero on entry and exit
+  int64_t N, K;
+  int M;
+  int NRT;               // row tiles
+  int NCH;               // 512-K chunks per row
+  int NKB;               // 64-K blocks per row (K / 64)
+  long long units;       // NRT * NCH
+};
+
+// Unit u = (row tile u / NCH, chunk u % NCH).  The K-blocks of chunk c are
+// [8c, min(8c + 8, NKB)).
+__device__ __forceinline__ int mma_chunk_kbs(const GemvMmaParams &p, int c) { return min(8, p.NKB - 8 * c); }
+
 constexpr int kMmaWarps = 8;                 // compute warps (one 64-K column each)
 constexpr int kMmaThreads = (kMmaWarps + 1) * 32;
-constexpr int kMmaStages = 5;
+// NT8 token tiles of 8.  CTAs per SM: two for 8 token rows (fits 96
+// registers: measured 1.2x), else one.  Stages: as many as shared memory
+// holds beside the reduction buffer.  WIDE (32 or 64 tokens): warp w owns row
+// block w over all K-blocks of a unit (the accumulators of 8 row blocks would
+// not fit in registers); otherwise warp w owns the 64-K column w of all 8 row
+// blocks.
+template <int NT8> struct MmaCfg {
+  static constexpr int ctas = NT8 == 1 ? 2 : 1;
+  static constexpr int stages = NT8 == 1 ? 3 : (NT8 == 2 ? 5 : (NT8 == 4 ? 3 : 2));
+  static constexpr bool wide = NT8 >= 4;
+};
 constexpr int kMmaBar = 3;                   // named barrier of the compute warps
 
 template <int NT8>
 struct GemvMmaSmem {
   static constexpr int kTok = NT8 * 8;                  // token rows of the B box
   static constexpr int kBBytes = 8 * kTok * 128;        // activation slice of a unit
+  static constexpr int kBoxRows = 8 * kTok < 256 ? 8 * kTok : 256;  // TMA box limit
   static constexpr int kStage = 16384 + kBBytes;
   static constexpr int ring = 0;
-  static constexpr int red = kMmaStages * kStage;       // [128 rows][M] int32
-  static constexpr int bars = red + 128 * 16 * 4;
-  static constexpr int flags = bars + 2 * kMmaStages * 8;
+  static constexpr int red = MmaCfg<NT8>::stages * kStage;       // [128 rows][M] int32
+  static constexpr int bars = red + 128 * kTok * 4;
+  static constexpr int flags = bars + 2 * MmaCfg<NT8>::stages * 8;
   static constexpr int bytes = flags + 16;
 };
 
 template <int NT8>
-__global__ void __launch_bounds__(kMmaThreads, 1)
+__global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap bmap,
-                    const GemvTcParams p) {
+                    const GemvMmaParams p) {
   using L = GemvMmaSmem<NT8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bars);
-  uint64_t *empty = full + kMmaStages;
+  uint64_t *empty = full + MmaCfg<NT8>::stages;
   int32_t *red = reinterpret_cast<int32_t *>(smem + L::red);
   volatile int *flags = reinterpret_cast<volatile int *>(smem + L::flags);  // [0] abort, [1] last CTA
 
@@ -72,7 +109,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const long long g1 = p.units * (blockIdx.x + 1) / gridDim.x;
   pdl_launch_dependents();
   if (tid == 0) {
-    for (int i = 0; i < kMmaStages; ++i) {
+    for (int i = 0; i < MmaCfg<NT8>::stages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kMmaWarps);
     }
@@ -92,8 +129,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       long long it = 0;
       bool waited = false;
       for (long long u = g0; u < g1; ++u, ++it) {
-        const int s = (int)(it % kMmaStages);
-        if (it >= kMmaStages && !mbar_wait(&empty[s], (uint32_t)(((it / kMmaStages) - 1) & 1))) {
+        const int s = (int)(it % MmaCfg<NT8>::stages);
+        if (it >= MmaCfg<NT8>::stages && !mbar_wait(&empty[s], (uint32_t)(((it / MmaCfg<NT8>::stages) - 1) & 1))) {
           raise_device_error(kDevErrTimeout);
           flags[0] = 1;
         }
@@ -106,13 +143,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           pdl_wait_prior_grid();
           waited = true;
         }
-        // the unit's 8 K-blocks x kTok token rows: one box (rows past K are zero-filled)
-        tma_load_2d(st + 16384, &bmap, &full[s], 0, c * 8 * L::kTok, pol_b);
+        // the unit's 8 K-blocks x kTok token rows: one box, two for 64 tokens
+        // (rows past K are zero-filled)
+        for (int b = 0; b < 8 * L::kTok; b += L::kBoxRows)
+          tma_load_2d(st + 16384 + b * 128, &bmap, &full[s], 0, c * 8 * L::kTok + b, pol_b);
       }
       if (!waited) pdl_wait_prior_grid();
       if (flags[0]) {  // leave no copy in flight (bounded waits)
-        for (long long j = (it > kMmaStages ? it - kMmaStages : 0); j < it; ++j)
-          mbar_wait(&full[j % kMmaStages], (uint32_t)((j / kMmaStages) & 1));
+        for (long long j = (it > MmaCfg<NT8>::stages ? it - MmaCfg<NT8>::stages : 0); j < it; ++j)
+          mbar_wait(&full[j % MmaCfg<NT8>::stages], (uint32_t)((j / MmaCfg<NT8>::stages) & 1));
       }
     }
     return;
@@ -121,10 +160,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   // ---------------------------------------------------------- compute warps --
   pdl_wait_prior_grid();  // xsum / fscale come from the previous kernel
   const int g = lane >> 2, t = lane & 3;
-  const int kb = warp;  // this warp's 64-K column of every unit
-  float d[8][NT8][4];
+  constexpr bool kWide = MmaCfg<NT8>::wide;
+  constexpr int RBN = kWide ? 1 : 8;  // row blocks in this warp's accumulators
+  const int kb = warp;                // narrow: this warp's 64-K column of every unit
+  float d[RBN][NT8][4];
 #pragma unroll
-  for (int rb = 0; rb < 8; ++rb)
+  for (int rb = 0; rb < RBN; ++rb)
 #pragma unroll
     for (int nt = 0; nt < NT8; ++nt)
 #pragma unroll
@@ -139,13 +180,49 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const long long u_end = tile_end < g1 ? tile_end : g1;  // segment: units [u, u_end) of tile r
     const int nch = (int)(u_end - u);
     for (; u < u_end; ++u, ++it) {
-      const int s = (int)(it % kMmaStages);
-      if (!flags[0] && !mbar_wait(&full[s], (uint32_t)((it / kMmaStages) & 1))) {
+      const int s = (int)(it % MmaCfg<NT8>::stages);
+      if (!flags[0] && !mbar_wait(&full[s], (uint32_t)((it / MmaCfg<NT8>::stages) & 1))) {
         raise_device_error(kDevErrTimeout);
         flags[0] = 1;
       }
       const int c = (int)(u % p.NCH);
-      if (kb < tc_chunk_kbs(p, c)) {
+      if constexpr (kWide) {
+        // row block `warp` over the unit's K-blocks
+        const uint32_t st = smem_u32(smem + L::ring + s * L::kStage);
+        const int r0 = warp * 16 + g;
+        const int nkb = mma_chunk_kbs(p, c);
+#pragma unroll 1
+        for (int k2 = 0; k2 < nkb; ++k2) {
+          const uint32_t off = (uint32_t)((((k2 ^ g) & 7) << 4) + (t << 2));
+          const uint32_t w0 = lds_u32(st + r0 * 128 + off);
+          const uint32_t w1 = lds_u32(st + (r0 + 8) * 128 + off);
+          const uint32_t bst = st + 16384 + k2 * L::kTok * 128;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t a0, a1, a2, a3;
+            if (j < 3) {
+              const uint32_t m0 = 0x00030003u << (4 * j), m1 = 0x00030003u << (4 * j + 2);
+              a0 = w0 & m0;
+              a1 = w1 & m0;
+              a2 = w0 & m1;
+              a3 = w1 & m1;
+            } else {
+              const uint32_t h0 = w0 >> 12, h1 = w1 >> 12;
+              a0 = h0 & 0x00030003u;
+              a1 = h1 & 0x00030003u;
+              a2 = h0 & 0x000C000Cu;
+              a3 = h1 & 0x000C000Cu;
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT8; ++nt) {
+              const int tok = nt * 8 + g;
+              const int ci = t * 2 + (j >> 1);
+              const uint2 bv = lds_u64(bst + tok * 128 + (((ci ^ (tok & 7)) & 7) << 4) + ((j & 1) << 3));
+              mma_f16_16816(d[0][nt], a0, a1, a2, a3, bv.x, bv.y);
+            }
+          }
+        }
+      } else if (kb < mma_chunk_kbs(p, c)) {
         const uint32_t st = smem_u32(smem + L::ring + s * L::kStage);
         uint32_t w0[8], w1[8];
 #pragma unroll
@@ -193,18 +270,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
 
     // ------------------------------------------------------- segment end --
-    // exact int32 partial sums of this warp's column into red[row][token]
+    // exact int32 partial sums into red[row][token]: added across the column
+    // warps; stored by the row-block owner in the wide form
 #pragma unroll
-    for (int rb = 0; rb < 8; ++rb)
+    for (int rb = 0; rb < RBN; ++rb)
 #pragma unroll
       for (int nt = 0; nt < NT8; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int row = rb * 16 + g + ((e >> 1) << 3);
+          const int row = (kWide ? warp : rb) * 16 + g + ((e >> 1) << 3);
           const int tok = nt * 8 + 2 * t + (e & 1);
           const int v = __float2int_rn(d[rb][nt][e] * 16777216.0f);
           d[rb][nt][e] = 0.0f;
-          if (tok < p.M && v != 0) atomicAdd(&red[row * p.M + tok], v);
+          if (tok < p.M) {
+            if (kWide)
+              red[row * p.M + tok] = v;
+            else if (v != 0)
+              atomicAdd(&red[row * p.M + tok], v);
+          }
         }
     named_barrier_sync(kMmaBar, kMmaWarps * 32);
     const bool whole = (c0 == 0) && (nch == p.NCH);

@@ -34,6 +34,7 @@ constexpr size_t kPackScratchHeader = 256;
 template <typename T>
 __global__ void __launch_bounds__(kPackThreads) pack_chunk_sums_kernel(const T *__restrict__ w, int64_t n,
                                                                        double *__restrict__ sums) {
+  pdl_wait_prior_grid();  // W may come from the previous kernel (launched with PDL)
   const int64_t c = (int64_t)blockIdx.x * kPackThreads + threadIdx.x;
   const int64_t c0 = c * kAbsChunk;
   if (c0 >= n) return;
@@ -45,6 +46,7 @@ __global__ void __launch_bounds__(kPackThreads) pack_chunk_sums_kernel(const T *
 
 __global__ void pack_finalize_kernel(const double *__restrict__ sums, int64_t nchunks, int64_t n, float alpha,
                                      float eps, PackScratch *scr, float *absmean_out) {
+  pdl_wait_prior_grid();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   double total = 0.0;
   for (int64_t c = 0; c < nchunks; ++c) total = __dadd_rn(total, sums[c]);
@@ -69,6 +71,7 @@ __device__ __forceinline__ uint32_t ternary_code(float gamma, float w) {
 template <typename T, bool WORD_STORE>
 __global__ void __launch_bounds__(kPackThreads) pack_codes_kernel(const T *__restrict__ w, int64_t n,
                                                                   uint8_t *__restrict__ packed, PackScratch *scr) {
+  pdl_wait_prior_grid();
   const float gamma = scr->gamma;
   const int64_t nwords = n / 16;
   unsigned cnt = 0;
@@ -109,7 +112,49 @@ __global__ void __launch_bounds__(kPackThreads) pack_codes_kernel(const T *__res
   if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(&scr->nnz, (unsigned long long)cnt);
 }
 
+// Group-wise scales (BitNet 深度拆解 §4.3: groups of group_size weights, each
+// with its own gamma and beta; one group per row is the per-channel scale):
+// group g of row n is W[n, gG .. gG + G - 1].  One thread per group does what
+// the four kernels above do for a whole matrix, in the same order: the fp64
+// sum of |w| in 4096-element chunks left to right, mean, gamma, the codes of
+// the group (G / 4 bytes, G % 4 == 0) and beta_g = nnz_g / G.
+template <typename T>
+__global__ void __launch_bounds__(kPackThreads) pack_grouped_kernel(const T *__restrict__ w, int64_t groups,
+                                                                    int64_t G, float alpha, float eps,
+                                                                    uint8_t *__restrict__ packed,
+                                                                    float *__restrict__ w_scale,
+                                                                    float *__restrict__ absmean) {
+  pdl_wait_prior_grid();
+  const int64_t gi = (int64_t)blockIdx.x * kPackThreads + threadIdx.x;
+  if (gi >= groups) return;
+  const T *wg = w + gi * G;  // groups are consecutive in the row-major matrix
+  double total = 0.0;
+  for (int64_t c0 = 0; c0 < G; c0 += kAbsChunk) {
+    const int64_t c1 = c0 + kAbsChunk < G ? c0 + kAbsChunk : G;
+    double part = 0.0;
+    for (int64_t i = c0; i < c1; ++i) part = __dadd_rn(part, (double)fabsf(load_as_f32(wg, i)));
+    total = __dadd_rn(total, part);
+  }
+  const float mean = __double2float_rn(__ddiv_rn(total, (double)G));
+  const float gamma = __fdiv_rn(1.0f, __fadd_rn(__fmul_rn(alpha, mean), eps));
+  uint8_t *pg = packed + gi * (G / 4);
+  int64_t nnz = 0;
+  for (int64_t b = 0; b < G / 4; ++b) {
+    uint32_t byte = 0;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const uint32_t code = ternary_code(gamma, load_as_f32(wg, 4 * b + s));
+      nnz += code != 1u;
+      byte |= code << (2 * s);
+    }
+    pg[b] = static_cast<uint8_t>(byte);
+  }
+  w_scale[gi] = __double2float_rn(__ddiv_rn((double)nnz, (double)G));
+  if (absmean) absmean[gi] = mean;
+}
+
 __global__ void pack_beta_kernel(const PackScratch *scr, int64_t n, float *beta) {
+  pdl_wait_prior_grid();
   if (threadIdx.x == 0 && blockIdx.x == 0) *beta = __double2float_rn(__ddiv_rn((double)scr->nnz, (double)n));
 }
 

@@ -128,7 +128,8 @@ class Workload:
 
 
 def workload(name: str) -> Workload:
-    """The five workloads (sizes, distributions and seeds)."""
+    """The workloads (sizes, distributions and seeds): the five matmul
+    workloads and the feed-forward decode built on them."""
     if name == "bitlinear-1024":
         return Workload(name, "single BitLinear decode: W N(0,0.02) [1024,1024], x fp32 N(0,1) [1,1024]", [1],
                         [Layer("linear", 1024, 1024, "normal", 0.02, 0, "normal", 0, x_bf16=False)])
@@ -145,6 +146,11 @@ def workload(name: str) -> Workload:
         return Workload(name, "prefill GEMM M=2048, Student-t(4) bf16 activations",
                         [2048], [Layer("k2560_n6912", 6912, 2560, "normal", 0.02, 40, "student_t4", 42),
                                  Layer("k6912_n2560", 2560, 6912, "normal", 0.02, 41, "student_t4", 43)])
+    if name == "ffn-2b-decode":
+        return Workload(name, "2B-shaped feed-forward decode: silu(gate(h)) * up(h) from the fused gate+up matrix "
+                              "[13824, 2560], then down [2560, 6912]; h bf16 N(0,1) with 0.1% x20 outliers",
+                        [1], [Layer("gate_up", 13824, 2560, "normal", 0.02, 50, "normal", 51, outlier_p=0.001),
+                              Layer("down", 2560, 6912, "normal", 0.02, 52, "normal", 53)])
     if name == "100b-stream":
         return Workload(name, "100B-class layer stream: 30 GEMVs N=28672, K=8192, Laplace(0,0.01) weights",
                         [1, 16], [Layer(f"layer{i}", 28672, 8192, "laplace", 0.01, 100 + i, "normal", 99)
@@ -152,4 +158,4 @@ def workload(name: str) -> Workload:
     raise KeyError(name)
 
 
-WORKLOADS = ["bitlinear-1024", "2b-decode", "gateup-sweep", "prefill-2048", "100b-stream"]
+WORKLOADS = ["bitlinear-1024", "2b-decode", "gateup-sweep", "prefill-2048", "100b-stream", "ffn-2b-decode"]

@@ -101,6 +101,83 @@ def test_matmul_validation(clib, fn):
         assert call(M=65) == SHAPE
 
 
+ALIGNMENT = 3
+
+
+def test_bitlinear_validation(clib):
+    nb = clib.bitnet_bitlinear_workspace_bytes(1, 8, 64)
+    assert nb > 0 and clib.bitnet_bitlinear_workspace_bytes(1, 8, 6) == 0
+
+    def call(x=FAKE, dt=1, M=1, p=FAKE, w=FAKE, N=8, K=64, y=FAKE, work=FAKE, wb=nb):
+        return clib.bitnet_bitlinear(x, dt, M, p, w, N, K, y, None, None, None, work, wb, None)
+
+    assert call(x=None) == INVALID_ARG
+    assert call(y=None) == INVALID_ARG
+    assert call(dt=2) == INVALID_ARG
+    assert call(M=0) == SHAPE
+    assert call(K=10) == SHAPE
+    assert call(x=FAKE + 1) == ALIGNMENT
+    assert call(work=None) == WORKSPACE
+    assert call(wb=nb - 1) == WORKSPACE
+    assert call(work=FAKE + 16) == WORKSPACE  # not 256-byte aligned
+
+
+def test_bitlinear_swiglu_validation(clib):
+    nb = clib.bitnet_bitlinear_swiglu_workspace_bytes(2, 8, 64)
+    # the fallback's two [M, I] fp32 outputs come on top of the BitLinear's
+    assert nb >= clib.bitnet_bitlinear_workspace_bytes(2, 8, 64) + 2 * 2 * 8 * 4
+    assert clib.bitnet_bitlinear_swiglu_workspace_bytes(0, 8, 64) == 0
+
+    def call(x=FAKE, dt=0, M=2, pg=FAKE, wg=FAKE, pu=FAKE, wu=FAKE, I=8, K=64, out=FAKE, work=FAKE, wb=nb):
+        return clib.bitnet_bitlinear_swiglu(x, dt, M, pg, wg, pu, wu, I, K, out, None, None, None, None, work, wb,
+                                            None)
+
+    for kw in ("x", "pg", "wg", "pu", "wu", "out"):
+        assert call(**{kw: None}) == INVALID_ARG, kw
+    assert call(dt=7) == INVALID_ARG
+    assert call(M=-1) == SHAPE
+    assert call(I=0) == SHAPE
+    assert call(K=66) == SHAPE
+    assert call(wu=FAKE + 2) == ALIGNMENT
+    assert call(work=None) == WORKSPACE
+    assert call(wb=nb - 1) == WORKSPACE
+
+
+def test_grouped_validation(clib):
+    def pack(W=FAKE, dt=0, N=4, K=256, G=128, p=FAKE, w=FAKE):
+        return clib.bitnet_pack_weights_grouped(W, dt, N, K, G, 1.0, 1e-8, p, w, None, None)
+
+    assert pack(W=None) == INVALID_ARG
+    assert pack(w=None) == INVALID_ARG
+    assert pack(dt=9) == INVALID_ARG
+    assert pack(G=0) == SHAPE
+    assert pack(G=6) == SHAPE      # not a multiple of 4
+    assert pack(G=96) == SHAPE     # does not divide K
+    assert pack(w=FAKE + 2) == ALIGNMENT
+
+    def mm(xq=FAKE, s=FAKE, M=1, p=FAKE, w=FAKE, N=8, K=256, G=64, y=FAKE):
+        return clib.bitnet_w2a8_grouped(xq, s, M, p, w, N, K, G, y, None, None)
+
+    assert mm(xq=None) == INVALID_ARG
+    assert mm(w=None) == INVALID_ARG
+    assert mm(M=0) == SHAPE
+    assert mm(G=48) == SHAPE
+    assert mm(y=FAKE + 1) == ALIGNMENT
+
+    nb = clib.bitnet_bitlinear_grouped_workspace_bytes(2, 256)
+    assert nb >= 2 * 256 + 8 and clib.bitnet_bitlinear_grouped_workspace_bytes(0, 256) == 0
+
+    def bl(x=FAKE, dt=1, M=2, G=64, work=FAKE, wb=nb):
+        return clib.bitnet_bitlinear_grouped(x, dt, M, FAKE, FAKE, 8, 256, G, FAKE, None, None, None, work, wb, None)
+
+    assert bl(x=None) == INVALID_ARG
+    assert bl(dt=3) == INVALID_ARG
+    assert bl(G=100) == SHAPE
+    assert bl(x=FAKE + 1) == ALIGNMENT
+    assert bl(work=None) == WORKSPACE
+    assert bl(wb=nb - 1) == WORKSPACE
+
+
 def test_workspace_sizes_cover_partials(clib):
     for M, N, K in [(1, 2560, 2560), (16, 28672, 8192), (64, 13824, 2560), (3, 129, 1000)]:
         nb = clib.bitnet_gemv_workspace_bytes(M, N, K)

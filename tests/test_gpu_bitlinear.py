@@ -37,7 +37,7 @@ def run_case(lib, oracle_mod, dev, M, N, K, dtype, seed, zero_row=False, dist="s
     return y
 
 
-# fused row-range kernel (M <= 2), fused prep + tcgen05 GEMV (3..64), fused
+# fused streaming kernel (M <= 2), fused prep + mma.sync GEMV (3..64), fused
 # prep + tcgen05 GEMM (> 64); ragged N, K not a multiple of 512
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("M", [1, 2, 3, 16, 64, 65, 300])

@@ -121,6 +121,23 @@ def test_pack_all_zero_and_ties(lib, oracle_mod, cuda_dev):
     assert np.array_equal(p.cpu().numpy().ravel(), p_ref) and b.item() == float(b_ref)
 
 
+def test_pack_with_pdl_enabled(lib, oracle_mod, cuda_dev):
+    """The four pack kernels launched with programmatic dependent launch:
+    each waits for its predecessor (absmean sums -> gamma -> codes -> beta),
+    repeated back to back on one stream."""
+    W = synth.weights_np(1000, 4096, "laplace", 0.01, seed=3)
+    p_ref, b_ref, am_ref = oracle_mod.pack_weights(W)
+    Wd = to_dev(W, cuda_dev)
+    lib.set_pdl(True)
+    try:
+        outs = [lib.pack_weights(Wd) for _ in range(4)]
+    finally:
+        lib.set_pdl(False)
+    for packed, beta, am in outs:
+        assert np.array_equal(packed.cpu().numpy().ravel(), p_ref)
+        assert beta.item() == float(b_ref) and am.item() == float(am_ref)
+
+
 # ------------------------------------------------------------------ GEMV ---
 
 def gemv_case(lib, oracle_mod, dev, M, N, K, seed, offset=0):

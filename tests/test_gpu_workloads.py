@@ -9,6 +9,7 @@ outputs the oracle computes row by row (every sampled row for every token):
   100b-stream     30 x (28672x8192), M in {1,16}                 pack of layers 0/29
                                                                  byte-exact, beta of
                                                                  all 30, 256 rows
+  ffn-2b-decode   gate+up 13824x2560 -> SwiGLU -> down 2560x6912 full (graph, PDL)
 Also the decode stack in the launch configuration the benchmark times
 (CUDA graph replay with programmatic dependent launch).
 """
@@ -163,4 +164,65 @@ def test_decode_stack_graph_launch(lib, oracle_mod, cuda_dev, pdl):
         p_ref, b_ref, _ = oracle_mod.pack_weights(e["W"])
         y_ref, _, _, _ = oracle_mod.bitlinear(e["xf"], p_ref, b_ref, L.N, L.K, threads=8)
         assert_y_close(e["y"].cpu().numpy(), y_ref)
+    lib.check_device_error()
+
+
+@pytest.mark.parametrize("M", [1, 2, 4])
+def test_ffn_2b_decode_graph_launch(lib, oracle_mod, cuda_dev, M):
+    """Two layers of the feed-forward decode workload (fused gate+up matrix,
+    SwiGLU, down) captured in a CUDA graph with programmatic dependent launch
+    and replayed three times, against the oracle: the SwiGLU product within
+    its bound, the down output within its bound given the near-midpoint
+    positions of its quantisation."""
+    import torch
+    from test_gpu_swiglu import assert_down_close, assert_swiglu_close, down_reference
+
+    wl = synth.workload("ffn-2b-decode")
+    gu, dn = wl.layers
+    I, D = gu.N // 2, gu.K
+    h = I * D // 4
+    layers = []
+    for rep in range(2):
+        Wgu = synth.weights_np(gu.N, gu.K, gu.w_dist, gu.w_scale, seed=gu.w_seed + 1000 * rep)
+        Wd = synth.weights_np(dn.N, dn.K, dn.w_dist, dn.w_scale, seed=dn.w_seed + 1000 * rep)
+        bits, xf = synth.acts_np(M, D, gu.x_dist, seed=gu.x_seed + 1000 * rep, outlier_p=gu.outlier_p)
+        pgu, bgu, _ = lib.pack_weights(to_dev(Wgu, cuda_dev))
+        pd, bd, _ = lib.pack_weights(to_dev(Wd, cuda_dev))
+        layers.append(dict(Wgu=Wgu, Wd=Wd, xf=xf, pg=pgu[:I], pu=pgu[I:], bgu=bgu, pd=pd, bd=bd,
+                           x=to_dev(bits, cuda_dev, torch.bfloat16),
+                           a=torch.empty((M, I), dtype=torch.float32, device=cuda_dev),
+                           y=torch.empty((M, D), dtype=torch.float32, device=cuda_dev)))
+    ws = torch.zeros(max(lib.bitlinear_swiglu_workspace_bytes(M, I, D), lib.bitlinear_workspace_bytes(M, D, I)),
+                     dtype=torch.uint8, device=cuda_dev)
+    stream = torch.cuda.Stream(cuda_dev)
+    lib.set_pdl(True)
+    try:
+        with torch.cuda.stream(stream):
+            def step():
+                for e in layers:
+                    lib.bitlinear_swiglu(e["x"], e["pg"], e["bgu"], e["pu"], e["bgu"], I, D, out=e["a"],
+                                         workspace=ws)
+                    lib.bitlinear(e["a"], e["pd"], e["bd"], D, I, out=e["y"], workspace=ws)
+
+            step()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step()
+            for e in layers:
+                e["a"].fill_(float("nan"))
+                e["y"].fill_(float("nan"))
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize(cuda_dev)
+    finally:
+        lib.set_pdl(False)
+    for e in layers:
+        pgu_ref, b_ref, _ = oracle_mod.pack_weights(e["Wgu"])
+        pd_ref, bd_ref, _ = oracle_mod.pack_weights(e["Wd"])
+        a_ref, accg_ref, _, _, s_ref = oracle_mod.bitlinear_swiglu(e["xf"], pgu_ref[:h], b_ref, pgu_ref[h:], b_ref,
+                                                                   I, D, threads=8)
+        assert_swiglu_close(e["a"].cpu().numpy(), a_ref, accg_ref, s_ref, float(b_ref))
+        dref = down_reference(oracle_mod, dict(a=a_ref, acc_g=accg_ref, s=s_ref, beta_g=float(b_ref)), pd_ref,
+                              bd_ref, D, I)
+        assert_down_close(e["y"].cpu().numpy(), dref, dref["near"].sum(axis=1))
     lib.check_device_error()
