@@ -265,3 +265,24 @@ def bitlinear_grouped(x: np.ndarray, packed: np.ndarray, w_scale: np.ndarray, N:
     acc_g = contract_grouped(xq, packed, N, K, G, threads=threads)
     y, cond = epilogue_grouped(acc_g, s, w_scale)
     return y, cond, acc_g, xq, s
+
+
+def bitlinear_fake_quant(W: np.ndarray, x: np.ndarray, weight_scale=None, alpha: float = 1.0, eps: float = 1e-8,
+                         threads: int = 1):
+    """The training-time BitLinear forward of [Deep-dive] section 3.1: the fp32
+    shadow weights are ternarised on every call (absmean, section 2.2), the
+    activations absmax-quantised, the integer product rescaled by act_scale
+    (absmax / 127) and by the per-output weight_scale (a learned [N] vector;
+    beta when None).  The straight-through estimator of section 2.4 only
+    changes the backward pass.  Returns (y, cond, acc, xq, s, packed, beta):
+    y fp64 with cond = |y| bound input as in epilogue_grouped when
+    weight_scale is given, else y fp32 rounded once (epilogue) and cond None."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    N, K = W.shape
+    packed, beta, _ = pack_weights(W, alpha, eps)
+    if weight_scale is None:
+        y, acc, xq, s = bitlinear(x, packed, beta, N, K, threads=threads)
+        return y, None, acc, xq, s, packed, beta
+    ws = np.ascontiguousarray(weight_scale, dtype=np.float32).reshape(N, 1)
+    y, cond, acc_g, xq, s = bitlinear_grouped(x, packed, ws, N, K, K, threads=threads)
+    return y, cond, acc_g[:, :, 0], xq, s, packed, beta

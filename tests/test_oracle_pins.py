@@ -473,3 +473,43 @@ def test_grouped_matmul_equals_dense_dequantised_fp64(oracle_mod, M, N, K, G):
     y1, _ = oracle_mod.epilogue_grouped(acc_g, s, ws1)
     acc = oracle_mod.contract(xq, packed, N, K)
     assert np.allclose(y1, acc * 0.625 * s.astype(np.float64)[:, None] / 127.0, rtol=1e-14, atol=0)
+
+
+# ------------------------------------- fake-quant (training) forward, NEXT-4 --
+
+@pytest.mark.parametrize("learned", [False, True])
+def test_fake_quant_forward_matches_page_torch_module(oracle_mod, learned):
+    """The training BitLinear module of BitNet 深度拆解 section 3.1 written out
+    in torch CPU ops (fp32 shadow weight, torch mean for absmean, torch.round,
+    F.linear of the integer-valued operands, out * act_scale * weight_scale
+    with act_scale = absmax / 127) against the oracle's composition."""
+    import torch
+    import torch.nn.functional as F
+
+    rng = np.random.default_rng(21 + learned)
+    M, N, K = 3, 64, 320
+    W = (rng.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32)  # the module's init scale
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    ws = (rng.standard_normal(N) * 0.5 + 1.0).astype(np.float32) if learned else None
+    y, cond, acc, xq, s, packed, beta = oracle_mod.bitlinear_fake_quant(W, x, ws)
+
+    Wt = torch.from_numpy(W)
+    gamma = 1.0 / (1.0 * Wt.abs().mean() + 1e-8)
+    w_t = torch.clamp(torch.round(Wt * gamma), -1, 1)
+    beta_t = w_t.abs().mean()
+    xt = torch.from_numpy(x)
+    amax = xt.abs().amax(dim=-1, keepdim=True).clamp_min(1e-8)
+    x_q = torch.clamp(torch.round(xt / amax * 127), -127, 127)
+    out_q = F.linear(x_q, w_t)
+    scale_n = torch.from_numpy(ws).double() if learned else beta_t.double()
+    ref = out_q.double() * (amax.double() / 127.0) * scale_n
+
+    assert np.array_equal(w_t.numpy().astype(np.int8).ravel(), oracle_mod.unpack_codes(packed, N * K))
+    assert float(beta) == float(beta_t)
+    assert np.array_equal(x_q.numpy().astype(np.int8), xq)
+    assert np.array_equal(out_q.numpy(), acc.astype(np.float32))
+    if learned:
+        np.testing.assert_allclose(y, ref.numpy(), rtol=1e-12, atol=0)
+        assert np.all(cond >= np.abs(y) * (1 - 1e-12))
+    else:
+        np.testing.assert_allclose(y, ref.float().numpy(), rtol=3e-7, atol=0)
