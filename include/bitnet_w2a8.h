@@ -273,6 +273,37 @@ int bitnet_bitlinear_grouped(const void *x, int dtype, int64_t M, const uint8_t 
                              int8_t *x_q, float *scale, int32_t *acc_g, void *workspace,
                              size_t workspace_bytes, cudaStream_t stream);
 
+/* Workspace bytes bitnet_bitlinear_fake_quant needs. */
+size_t bitnet_bitlinear_fake_quant_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * bitnet_bitlinear_fake_quant -- the training-time BitLinear forward of
+ * [Deep-dive] §3.1: the fp32 (or bf16) shadow weights W are ternarised on
+ * every call (bitnet_pack_weights: absmean, §2.2), x is absmax-quantised per
+ * token, and the integer product is rescaled by s_m / 127 and by the
+ * per-output weight_scale[n] (the module's learned scale) -- or by beta when
+ * weight_scale is NULL.  The straight-through estimator of §2.4 only affects
+ * the backward pass, which this library does not compute.
+ * Results equal bitnet_pack_weights followed by bitnet_bitlinear (beta) or by
+ * bitnet_bitlinear_grouped with G = K (weight_scale).
+ *   W        device, [N, K] row-major, BITNET_F32 or BITNET_BF16.
+ *   x        device, [M, K], BITNET_F32 or BITNET_BF16.
+ *   alpha, eps: as bitnet_pack_weights.
+ *   weight_scale device, [N] float, or NULL (beta).
+ *   y        device, [M, N] float out.
+ *   packed, beta: device outs (N * K / 4 bytes, one float), or NULL (then in
+ *            the workspace).
+ *   x_q, scale, acc: device outs as bitnet_bitlinear, or NULL.
+ *   workspace device, >= bitnet_bitlinear_fake_quant_workspace_bytes(M, N, K),
+ *            256-byte aligned, any contents.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE, CUDA.
+ */
+int bitnet_bitlinear_fake_quant(const void *W, int w_dtype, const void *x, int x_dtype, int64_t M,
+                                int64_t N, int64_t K, float alpha, float eps,
+                                const float *weight_scale, float *y, uint8_t *packed, float *beta,
+                                int8_t *x_q, float *scale, int32_t *acc, void *workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
 /* Bytes of the fixed device array behind bitnet_w2a8_gemv_static_scratch. */
 #define BITNET_GEMV_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
 

@@ -334,3 +334,44 @@ def bitlinear_grouped(x: torch.Tensor, packed: torch.Tensor, w_scale: torch.Tens
 
 def bitlinear_grouped_workspace_bytes(M: int, K: int) -> int:
     return int(_L().bitnet_bitlinear_grouped_workspace_bytes(M, K))
+
+
+def bitlinear_fake_quant(W: torch.Tensor, x: torch.Tensor, weight_scale=None, alpha: float = 1.0, eps: float = 1e-8,
+                         want_acc: bool = False, want_packed: bool = False, out=None, workspace=None):
+    """Training-time BitLinear forward: the shadow weights W [N, K] (fp32/bf16)
+    are ternarised on this call, x [M, K] quantised per token, y fp32 [M, N]
+    rescaled by weight_scale [N] (learned per-output scale) or by beta.
+    With want_acc also the exact int32 products, with want_packed the packed
+    weights and beta of this call."""
+    for t, nm in ((W, "W"), (x, "x")):
+        _dev(t, nm)
+    if weight_scale is not None:
+        _dev(weight_scale, "weight_scale")
+    if W.dim() != 2 or x.dim() != 2:
+        raise ValueError("W must be [N, K] and x [M, K]")
+    N, K = W.shape
+    M = x.shape[0]
+    dev = x.device
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=dev)
+    acc = torch.empty((M, N), dtype=torch.int32, device=dev) if want_acc else None
+    packed = torch.empty((N, K // 4), dtype=torch.uint8, device=dev) if want_packed else None
+    beta = torch.empty(1, dtype=torch.float32, device=dev) if want_packed else None
+    nbytes = bitlinear_fake_quant_workspace_bytes(M, N, K)
+    stream = _stream(dev)
+    if workspace is None:
+        workspace = _ws.get(dev, "bitlinear_fake_quant", nbytes, stream)
+    ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+    st = _L().bitnet_bitlinear_fake_quant(W.data_ptr(), _dtype_code(W), x.data_ptr(), _dtype_code(x), M, N, K, alpha,
+                                          eps, ptr(weight_scale), y.data_ptr(), ptr(packed), ptr(beta), None, None,
+                                          ptr(acc), workspace.data_ptr(), workspace.numel(), stream)
+    _lib.check("bitnet_bitlinear_fake_quant", st)
+    res = (y,)
+    if want_acc:
+        res += (acc,)
+    if want_packed:
+        res += (packed, beta)
+    return res[0] if len(res) == 1 else res
+
+
+def bitlinear_fake_quant_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_L().bitnet_bitlinear_fake_quant_workspace_bytes(M, N, K))

@@ -230,6 +230,20 @@ bitnet_status launch_gemv_ldg(const int8_t *x_q, const float *scale, const void 
     p.G = (int)G;
     p.NG = (int)(K / G);
     p.P = (int)(G / 64);
+    // shifts for power-of-two groups; one group per row needs none (index 0)
+    int gs = 0;
+    while (((int64_t)1 << gs) < G) ++gs;
+    p.GS = p.NG == 1 ? 31 : gs;
+    p.PS = p.NG == 1 ? 0 : gs - 6;
+  }
+  int J = (int)cdiv(K / 64, 32);
+  if (GR && p.NG > 1 && p.P <= 4) {
+    // lane-local groups: P slots per group, groups lane, lane + 32, ...
+    const int jl = p.P * (int)cdiv(p.NG, 32);
+    if (jl <= (M == 1 ? 4 : 2)) {
+      p.LOCAL = 1;
+      J = jl;
+    }
   }
   p.packed_up = packed_up;
   p.w_scale_up = w_scale_up;
@@ -258,7 +272,6 @@ bitnet_status launch_gemv_ldg(const int8_t *x_q, const float *scale, const void 
   p.SR = (int)std::max<int64_t>(1, std::min<int64_t>(kLdgStageBytes / rowb, rpw));
   p.RS = (int)((p.SR * rowb + 15) & ~(int64_t)15);
   p.NS = (int)std::min<int64_t>(kLdgStages, cdiv(rpw, p.SR));
-  const int J = (int)cdiv(p.C, 32);
   const size_t smem = gemv_ldg_smem_layout((int)M, p.C, p.RS, p.NS, GR ? p.NG : 0).bytes + 128;
   auto run = [&](auto kernel) -> bitnet_status {
     if (set_smem(kernel, smem) != BITNET_OK) return BITNET_ERR_CUDA;
@@ -888,6 +901,50 @@ int bitnet_bitlinear_grouped(const void *x, int dtype, int64_t M, const uint8_t 
   float *s_buf = scale ? scale : reinterpret_cast<float *>(ws + (((size_t)M * (size_t)K + 255) & ~(size_t)255));
   if (int st = bitnet_quant_act(x, dtype, M, K, xq_buf, s_buf, stream)) return st;
   return bitnet_w2a8_grouped(xq_buf, s_buf, M, packed, w_scale, N, K, G, y, acc_g, stream);
+}
+
+// ------------------------------------------- training-time (fake-quant) BitLinear --
+
+namespace {
+size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
+}  // namespace
+
+size_t bitnet_bitlinear_fake_quant_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const size_t pk = bitnet_pack_workspace_bytes(N, K);
+  const size_t bl = bitnet_bitlinear_workspace_bytes(M, N, K);
+  const size_t gr = bitnet_bitlinear_grouped_workspace_bytes(M, K);
+  if (pk == 0 || bl == 0 || gr == 0) return 0;
+  return round256((size_t)(N * K / 4)) + 256 + std::max(pk, std::max(bl, gr));
+}
+
+int bitnet_bitlinear_fake_quant(const void *W, int w_dtype, const void *x, int x_dtype, int64_t M, int64_t N,
+                                int64_t K, float alpha, float eps, const float *weight_scale, float *y,
+                                uint8_t *packed, float *beta, int8_t *x_q, float *scale, int32_t *acc,
+                                void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!W || !x || !y) return BITNET_ERR_INVALID_ARG;
+  if ((w_dtype != BITNET_F32 && w_dtype != BITNET_BF16) || (x_dtype != BITNET_F32 && x_dtype != BITNET_BF16))
+    return BITNET_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha) || !std::isfinite(eps)) return BITNET_ERR_INVALID_ARG;
+  if (M <= 0 || !shape_ok(N, K) || M > kMaxElems / K || M > kMaxElems / N) return BITNET_ERR_SHAPE;
+  if (N > 0x7fffffff || K > 0x7fffffff || M > 0x7fffffff) return BITNET_ERR_SHAPE;
+  if (!aligned(beta, 4) || !aligned(weight_scale, 4) || !aligned(y, 4)) return BITNET_ERR_ALIGNMENT;
+  const size_t need = bitnet_bitlinear_fake_quant_workspace_bytes(M, N, K);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return BITNET_ERR_WORKSPACE;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  const size_t pbytes = round256((size_t)(N * K / 4));
+  uint8_t *pk = packed ? packed : ws;
+  float *bt = beta ? beta : reinterpret_cast<float *>(ws + pbytes);
+  float *am = reinterpret_cast<float *>(ws + pbytes + 128);
+  uint8_t *tail = ws + pbytes + 256;
+  const size_t tail_bytes = workspace_bytes - pbytes - 256;
+  // the shadow weights, ternarised and packed for this call ([Deep-dive] §2.2, §3.3)
+  if (int st = bitnet_pack_weights(W, w_dtype, N, K, alpha, eps, pk, bt, am, tail, tail_bytes, stream)) return st;
+  // the forward on them: with a per-output weight_scale (the training module's
+  // learned scale) as a one-group-per-row scale, else with beta
+  if (weight_scale)
+    return bitnet_bitlinear_grouped(x, x_dtype, M, pk, weight_scale, N, K, K, y, x_q, scale, acc, tail, tail_bytes,
+                                    stream);
+  return bitnet_bitlinear(x, x_dtype, M, pk, bt, N, K, y, x_q, scale, acc, tail, tail_bytes, stream);
 }
 
 int bitnet_check_device_error(cudaStream_t stream) {

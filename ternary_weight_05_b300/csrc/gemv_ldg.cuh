@@ -31,9 +31,13 @@
 //     group of G consecutive weights of a row has its own scale; G = K is a
 //     per-channel scale).  A stage also carries its rows' scales (cp.async,
 //     4 bytes each, by all lanes); the per-group Σ x_q come from the
-//     prologue.  With P = G / 64 chunks per group (G <= 2048), aligned runs
-//     of P lanes add their chunk sums by shuffles and the run's first lane
-//     adds (acc_g) * scale_g into an fp32 partial; the warp then adds the
+//     prologue.  With P = G / 64 chunks per group and P <= 4 a lane owns
+//     whole groups: its chunk slots hold the P chunks of groups lane,
+//     lane + 32, ... (the order inside a group rotated per lane so that the
+//     warp's 16-byte reads hit distinct bank groups), it sums a group in
+//     registers and adds acc_g * scale_g into an fp32 partial.  For larger P
+//     (G <= 2048) aligned runs of P lanes add their chunk sums by shuffles
+//     and the run's first lane adds the term.  The warp then adds the
 //     partials and lane m writes F * (s_m / 127).  With one group per row the
 //     row sum is taken whole.
 #pragma once
@@ -88,6 +92,8 @@ struct GemvLdgParams {
   int RS;  // bytes per stage (SR rows, a multiple of 16)
   int NS;  // stages per warp (<= kLdgStages)
   int G, NG, P;  // grouped form: group size, groups per row, 16-byte chunks per group
+  int GS, PS;    // log2 G and log2 P (G a power of two), or 31 / 0 with one group per row
+  int LOCAL;     // grouped form, P <= 4: each lane owns whole groups (see gemv_ldg_kernel)
 };
 
 // 4-byte asynchronous copy global -> shared (per-thread completion groups).
@@ -259,7 +265,7 @@ __global__ void __launch_bounds__(kLdgThreads, BITNET_LDG_MIN_CTAS) gemv_ldg_ker
         const int4 u = *reinterpret_cast<const int4 *>(p.xq + (int64_t)m * p.K + (int64_t)q * 16);
         memcpy(v, &u, 16);
         const int sum = rows_pack_group(v, xw + (size_t)m * p.C * 64 + (size_t)q * 16);
-        if (GR && sum) atomicAdd(&xsumg[m * p.NG + (q * 16) / p.G], sum);
+        if (GR && sum) atomicAdd(&xsumg[m * p.NG + ((q * 16) >> p.GS)], sum);
 #pragma unroll
         for (int mm = 0; mm < MT; ++mm)
           if (mm == m) part[mm] += sum;
@@ -283,7 +289,7 @@ __global__ void __launch_bounds__(kLdgThreads, BITNET_LDG_MIN_CTAS) gemv_ldg_ker
             *reinterpret_cast<int4 *>(p.xq_out + (int64_t)m * p.K + (int64_t)q * 16) = u;
           }
           const int sum = rows_pack_group(v, xw + (size_t)m * p.C * 64 + (size_t)q * 16);
-          if (GR && sum) atomicAdd(&xsumg[m * p.NG + (q * 16) / p.G], sum);
+          if (GR && sum) atomicAdd(&xsumg[m * p.NG + ((q * 16) >> p.GS)], sum);
 #pragma unroll
           for (int mm = 0; mm < MT; ++mm)
             if (mm == m) part[mm] += sum;
@@ -300,13 +306,23 @@ __global__ void __launch_bounds__(kLdgThreads, BITNET_LDG_MIN_CTAS) gemv_ldg_ker
   }
   __syncthreads();
 
-  // this lane's activation words, for chunks lane + 32 j
+  // the chunk of each of this lane's slots: lane + 32 j, or with lane-local
+  // groups chunk P q + ((j % P + rot) % P) of group q = lane + 32 (j / P)
+  const bool local = GR && p.LOCAL;
+  int cj[J];
+  {
+    const int rot = local ? ((lane >> (3 - p.PS)) & (p.P - 1)) : 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+      cj[j] = local ? p.P * (lane + 32 * (j >> p.PS)) + (((j & (p.P - 1)) + rot) & (p.P - 1)) : lane + 32 * j;
+  }
+  // this lane's activation words, for its chunks
   uint32_t xr[MT][J][16];
 #pragma unroll
   for (int m = 0; m < MT; ++m)
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-      const int c = lane + 32 * j;
+      const int c = cj[j];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -365,6 +381,17 @@ __global__ void __launch_bounds__(kLdgThreads, BITNET_LDG_MIN_CTAS) gemv_ldg_ker
   // grouped form: the fp32 sum over the row's groups of acc_g * scale_g, per
   // token (every lane ends with the totals).  `sc` holds the row's NG scales;
   // with `accg` non-null the per-group products go to accg[(m * N + r) * NG + g].
+  // per lane and chunk column j: its group, whether it leads the run of P
+  // lanes, and the group's sum of x_q (constant over rows)
+  int gj[J];
+  int32_t xsg[MT][J];
+  const bool lead = GR && (lane & (p.P - 1)) == 0;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    gj[j] = !GR ? 0 : (local ? lane + 32 * (j >> p.PS) : (lane + 32 * j) >> p.PS);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) xsg[m][j] = (GR && gj[j] < p.NG) ? xsumg[m * p.NG + gj[j]] : 0;
+  }
   auto row_grouped = [&](const uint8_t *row, const float *sc, int64_t r, float (&F)[MT]) {
     float f[MT];
 #pragma unroll
@@ -393,17 +420,74 @@ __global__ void __launch_bounds__(kLdgThreads, BITNET_LDG_MIN_CTAS) gemv_ldg_ker
         }
       }
       // this chunk's sum of code * x, then the run of P lanes of its group
-      const int g = c / p.P;
-      const bool lead = (lane & (p.P - 1)) == 0 && c < p.C;
+      const int g = gj[j];
+      const bool head = lead && c < p.C;
+      const float w = head ? sc[g] : 0.0f;
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
         int t = a[m][0] + (a[m][1] >> 2) + (a[m][2] >> 4) + (a[m][3] >> 6);
-        for (int o = 1; o < p.P; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-        if (lead) {
-          const int32_t ag = t - xsumg[m * p.NG + g];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1)
+          if (o < p.P) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (head) {
+          const int32_t ag = t - xsg[m][j];
           if (p.acc) p.acc[((int64_t)m * p.N + r) * p.NG + g] = ag;
-          f[m] = __fmaf_rn((float)ag, sc[g], f[m]);
+          f[m] = __fmaf_rn((float)ag, w, f[m]);
         }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float v = f[m];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+      F[m] = v;
+    }
+  };
+
+  // lane-local groups: the same sum with each group finished in registers
+  auto row_local = [&](const uint8_t *row, const float *sc, int64_t r, float (&F)[MT]) {
+    float f[MT];
+    int a[MT][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      f[m] = 0.0f;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) a[m][s] = 0;
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int c = cj[j];
+      uint4 wq = make_uint4(0u, 0u, 0u, 0u);
+      if (c < p.C) wq = lds_u128(smem_u32(row + (size_t)c * 16));
+      const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t f0 = wv[u] & 0x03030303u, f1 = wv[u] & 0x0C0C0C0Cu;
+        const uint32_t f2 = wv[u] & 0x30303030u, f3 = wv[u] & 0xC0C0C0C0u;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          a[m][0] = dp4a_u8s8(f0, xr[m][j][4 * u + 0], a[m][0]);
+          a[m][1] = dp4a_u8s8(f1, xr[m][j][4 * u + 1], a[m][1]);
+          a[m][2] = dp4a_u8s8(f2, xr[m][j][4 * u + 2], a[m][2]);
+          a[m][3] = dp4a_u8s8(f3, xr[m][j][4 * u + 3], a[m][3]);
+        }
+      }
+      if ((j & (p.P - 1)) == p.P - 1) {  // the group's last chunk
+        const int g = gj[j];
+        if (g < p.NG) {
+          const float w = sc[g];
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const int32_t ag = a[m][0] + (a[m][1] >> 2) + (a[m][2] >> 4) + (a[m][3] >> 6) - xsg[m][j];
+            if (p.acc) p.acc[((int64_t)m * p.N + r) * p.NG + g] = ag;
+            f[m] = __fmaf_rn((float)ag, w, f[m]);
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int s = 0; s < 4; ++s) a[m][s] = 0;
       }
     }
 #pragma unroll
@@ -449,7 +533,8 @@ __global__ void __launch_bounds__(kLdgThreads, BITNET_LDG_MIN_CTAS) gemv_ldg_ker
             }
         } else {
           float F[MT];
-          row_grouped(stage + (size_t)i * rowb, sc, r, F);
+          if (local) row_local(stage + (size_t)i * rowb, sc, r, F);
+          else row_grouped(stage + (size_t)i * rowb, sc, r, F);
 #pragma unroll
           for (int m = 0; m < MT; ++m)
             if (lane == m) p.y[(int64_t)m * p.N + r] = __fmul_rn(F[m], fs[m]);

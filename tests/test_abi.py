@@ -178,6 +178,26 @@ def test_grouped_validation(clib):
     assert bl(wb=nb - 1) == WORKSPACE
 
 
+def test_fake_quant_validation(clib):
+    nb = clib.bitnet_bitlinear_fake_quant_workspace_bytes(2, 8, 64)
+    assert nb >= 8 * 64 // 4 + clib.bitnet_bitlinear_workspace_bytes(2, 8, 64)
+    assert clib.bitnet_bitlinear_fake_quant_workspace_bytes(2, 8, 6) == 0
+
+    def call(W=FAKE, wd=0, x=FAKE, xd=1, M=2, N=8, K=64, a=1.0, e=1e-8, wsc=None, y=FAKE, work=FAKE, wb=nb):
+        return clib.bitnet_bitlinear_fake_quant(W, wd, x, xd, M, N, K, a, e, wsc, y, None, None, None, None, None,
+                                                work, wb, None)
+
+    assert call(W=None) == INVALID_ARG
+    assert call(x=None) == INVALID_ARG
+    assert call(wd=4) == INVALID_ARG
+    assert call(a=float("nan")) == INVALID_ARG
+    assert call(K=62) == SHAPE
+    assert call(M=0) == SHAPE
+    assert call(wsc=FAKE + 1) == ALIGNMENT
+    assert call(work=None) == WORKSPACE
+    assert call(wb=nb - 1) == WORKSPACE
+
+
 def test_workspace_sizes_cover_partials(clib):
     for M, N, K in [(1, 2560, 2560), (16, 28672, 8192), (64, 13824, 2560), (3, 129, 1000)]:
         nb = clib.bitnet_gemv_workspace_bytes(M, N, K)
