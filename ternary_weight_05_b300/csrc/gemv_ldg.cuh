@@ -213,23 +213,30 @@ __global__ void __launch_bounds__(kLdgThreads, BITNET_LDG_MIN_CTAS) gemv_ldg_ker
   }
   __syncthreads();
   const int groups = p.C * 4;  // 16-K groups per token
+  // Activation words of 16-K group q = 4 c + u (chunk c): word s holds the
+  // bytes x_q[16 q + 4 b + s], b = 0..3; the four words sit at granule
+  // u * C + c of the token's area, so that the lanes' 16-byte reads of one u
+  // (chunks lane + 32 j) are consecutive granules.
+  auto xw_group = [&](int m, int q) { return xw + (size_t)m * p.C * 64 + ((size_t)(q & 3) * p.C + (q >> 2)) * 16; };
   {
     float s[MT];
-    float f[kLdgGroups][16];  // fused forms: this thread's activation groups
+    // fused forms: each thread quantises 8-element halves of 16-K groups
+    // (up to kLdgGroups * 2 of them, kept in registers from the absmax on)
+    float f[2 * kLdgGroups][8];
     if constexpr (!std::is_same<XT, int8_t>::value) {
       const XT *x = static_cast<const XT *>(p.x);
       float amax[MT];
 #pragma unroll
       for (int m = 0; m < MT; ++m) amax[m] = 0.0f;
 #pragma unroll
-      for (int n = 0; n < kLdgGroups; ++n) {
+      for (int n = 0; n < 2 * kLdgGroups; ++n) {
         const int i = tid + n * kLdgThreads;
-        if (i < MT * groups) {
-          const int m = i / groups, q = i % groups;
-          rows_load16(x + (int64_t)m * p.K + (int64_t)q * 16, f[n]);
+        if (i < MT * groups * 2) {
+          const int m = i / (2 * groups), h = i % (2 * groups);
+          load8(x + (int64_t)m * p.K + (int64_t)h * 8, f[n]);
           float a = 0.0f;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) a = fmaxf(a, fabsf(f[n][e]));
+          for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(f[n][e]));
 #pragma unroll
           for (int mm = 0; mm < MT; ++mm)
             if (mm == m) amax[mm] = fmaxf(amax[mm], a);
@@ -264,7 +271,7 @@ __global__ void __launch_bounds__(kLdgThreads, BITNET_LDG_MIN_CTAS) gemv_ldg_ker
         int8_t v[16];
         const int4 u = *reinterpret_cast<const int4 *>(p.xq + (int64_t)m * p.K + (int64_t)q * 16);
         memcpy(v, &u, 16);
-        const int sum = rows_pack_group(v, xw + (size_t)m * p.C * 64 + (size_t)q * 16);
+        const int sum = rows_pack_group(v, xw_group(m, q));
         if (GR && sum) atomicAdd(&xsumg[m * p.NG + ((q * 16) >> p.GS)], sum);
 #pragma unroll
         for (int mm = 0; mm < MT; ++mm)
@@ -272,23 +279,31 @@ __global__ void __launch_bounds__(kLdgThreads, BITNET_LDG_MIN_CTAS) gemv_ldg_ker
       }
     } else {
 #pragma unroll
-      for (int n = 0; n < kLdgGroups; ++n) {
+      for (int n = 0; n < 2 * kLdgGroups; ++n) {
         const int i = tid + n * kLdgThreads;
-        if (i < MT * groups) {
-          const int m = i / groups, q = i % groups;
+        if (i < MT * groups * 2) {
+          const int m = i / (2 * groups), h = i % (2 * groups), q = h >> 1, half = h & 1;
           float sm = s[0];
 #pragma unroll
           for (int mm = 1; mm < MT; ++mm)
             if (mm == m) sm = s[mm];
-          int8_t v[16];
+          int8_t v[8];
+          int sum = 0;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = quantize_one(f[n][e], sm);
-          if (blockIdx.x == 0 && p.xq_out) {
-            int4 u;
-            memcpy(&u, v, 16);
-            *reinterpret_cast<int4 *>(p.xq_out + (int64_t)m * p.K + (int64_t)q * 16) = u;
+          for (int e = 0; e < 8; ++e) {
+            v[e] = quantize_one(f[n][e], sm);
+            sum += v[e];
           }
-          const int sum = rows_pack_group(v, xw + (size_t)m * p.C * 64 + (size_t)q * 16);
+          if (blockIdx.x == 0 && p.xq_out) {
+            uint2 u;
+            memcpy(&u, v, 8);
+            *reinterpret_cast<uint2 *>(p.xq_out + (int64_t)m * p.K + (int64_t)h * 8) = u;
+          }
+          // this half holds b = 2 half, 2 half + 1 of the group: bytes 2 half
+          // and 2 half + 1 of each of the four words
+          uint16_t *w16 = reinterpret_cast<uint16_t *>(xw_group(m, q)) + half;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) w16[2 * t] = (uint16_t)((uint8_t)v[t] | ((uint32_t)(uint8_t)v[4 + t] << 8));
           if (GR && sum) atomicAdd(&xsumg[m * p.NG + ((q * 16) >> p.GS)], sum);
 #pragma unroll
           for (int mm = 0; mm < MT; ++mm)
@@ -326,7 +341,7 @@ __global__ void __launch_bounds__(kLdgThreads, BITNET_LDG_MIN_CTAS) gemv_ldg_ker
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (c < p.C) v = *reinterpret_cast<const uint4 *>(xw + (size_t)m * p.C * 64 + (size_t)c * 64 + g * 16);
+        if (c < p.C) v = *reinterpret_cast<const uint4 *>(xw_group(m, 4 * c + g));
         xr[m][j][4 * g + 0] = v.x;
         xr[m][j][4 * g + 1] = v.y;
         xr[m][j][4 * g + 2] = v.z;
