@@ -64,7 +64,10 @@ constexpr int kLdgThreads = kLdgWarps * 32;
 // warps own (p.RS bytes x p.NS stages), so that small matrices leave room on
 // the SM for the next kernel's CTAs (programmatic dependent launch).
 constexpr int kLdgStageBytes = BITNET_LDG_STAGE_BYTES;  // per warp stage: whole rows
-constexpr int kLdgStages = 16384 / kLdgStageBytes;     // 16 KB of stages per warp
+#ifndef BITNET_LDG_RING_BYTES
+#define BITNET_LDG_RING_BYTES 16384
+#endif
+constexpr int kLdgStages = BITNET_LDG_RING_BYTES / kLdgStageBytes;  // stages per warp ring
 // Fused prologue: each thread keeps up to kLdgGroups 16-element activation
 // groups in registers between the absmax and the quantisation (one read of
 // x); the host only sends shapes with M * K / 16 <= kLdgGroups * kLdgThreads.
