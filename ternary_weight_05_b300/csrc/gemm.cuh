@@ -40,7 +40,11 @@ namespace bitnet {
 #define BITNET_GEMM_STAGES 4
 #endif
 constexpr int kGemmDecSets = BITNET_GEMM_DEC_SETS;  // decoder warp sets of 4 warps
-constexpr int kGemmThreads = 384 + (kGemmDecSets - 1) * 128;
+// Epilogue: two sets of four warps (one per TMEM lane quarter each), each set
+// taking half of the accumulator's token columns.
+constexpr int kGemmEpiSets = 2;
+constexpr int kGemmEpiWarp2 = 12 + (kGemmDecSets - 1) * 4;  // first warp of epilogue set 1
+constexpr int kGemmThreads = 384 + (kGemmDecSets - 1) * 128 + (kGemmEpiSets - 1) * 128;
 constexpr int kGemmRows = 128;   // weight rows per tile (MMA M)
 #ifndef BITNET_GEMM_TOK
 #define BITNET_GEMM_TOK 256
@@ -352,7 +356,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accfull[i], 1);
-      mbar_init(&accempty[i], 4);
+      mbar_init(&accempty[i], 4 * kGemmEpiSets);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -446,7 +450,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_commit(drain);
       mbar_wait(drain, 0);
     }
-  } else if ((warp >= 4 && warp < 8) || warp >= 12) {
+  } else if ((warp >= 4 && warp < 8) || (warp >= 12 && warp < kGemmEpiWarp2)) {
     // ---------------------------------------------------------- decoders --
     // tcgen05.st is warp-collective: the abort decision is made warp-uniform.
     pdl_wait_prior_grid();
@@ -501,10 +505,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-  } else if (warp >= 8 && warp < 12) {
+  } else if ((warp >= 8 && warp < 12) || warp >= kGemmEpiWarp2) {
     // ---------------------------------------------------------- epilogue --
     pdl_wait_prior_grid();
     const int quad = warp & 3, row = quad * 32 + lane;
+    const int eset = warp < 12 ? 0 : 1;  // which half of the token columns
     long long tc = 0;
     for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x, ++tc) {
       const int rt = (int)(t % p.NRT), tt = (int)(t / p.NRT);
@@ -514,19 +519,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const int64_t n = (int64_t)rt * kGemmRows + row;
 #pragma unroll 1
-      for (int cb = 0; cb < kGemmTok / 32; ++cb) {
+      for (int cb = eset * (kGemmTok / 64); cb < (eset + 1) * (kGemmTok / 64); ++cb) {
+        // lane j fetches token tok0 + j's sum and scale (one coalesced load
+        // each, issued before the TMEM load); the outputs take them by
+        // shuffles, so no load waits behind an output store
+        const int64_t tok0 = (int64_t)tt * kGemmTok + cb * 32;
+        const int32_t xs_l = tok0 + lane < p.M ? __ldg(p.xsum + tok0 + lane) : 0;
+        const float fs_l = tok0 + lane < p.M ? __ldg(p.fscale + tok0 + lane) : 0.0f;
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + kGemmAccCol + a * kGemmTok + cb * 32, r);
-        const int64_t tok0 = (int64_t)tt * kGemmTok + cb * 32;
-        if (n < p.N) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int64_t tok = tok0 + j;
-            if (tok < p.M) {
-              const int32_t v = __float2int_rn(__uint_as_float(r[j]) * 16777216.0f) - __ldg(p.xsum + tok);
-              if (p.acc) p.acc[tok * p.N + n] = v;
-              p.y[tok * p.N + n] = __fmul_rn((float)v, __ldg(p.fscale + tok));
-            }
+        for (int j = 0; j < 32; ++j) {
+          // shuffles by the whole warp (rows past N only skip the stores)
+          const int32_t xs = __shfl_sync(0xffffffffu, xs_l, j);
+          const float fs = __shfl_sync(0xffffffffu, fs_l, j);
+          const int64_t tok = tok0 + j;
+          if (n < p.N && tok < p.M) {
+            const int32_t v = __float2int_rn(__uint_as_float(r[j]) * 16777216.0f) - xs;
+            if (p.acc) p.acc[tok * p.N + n] = v;
+            p.y[tok * p.N + n] = __fmul_rn((float)v, fs);
           }
         }
       }
