@@ -40,9 +40,12 @@ namespace bitnet {
 #define BITNET_GEMM_STAGES 4
 #endif
 constexpr int kGemmDecSets = BITNET_GEMM_DEC_SETS;  // decoder warp sets of 4 warps
-// Epilogue: two sets of four warps (one per TMEM lane quarter each), each set
-// taking half of the accumulator's token columns.
-constexpr int kGemmEpiSets = 2;
+// Epilogue: sets of four warps (one per TMEM lane quarter each), each set
+// taking an equal share of the accumulator's 32-token column blocks.
+#ifndef BITNET_GEMM_EPI_SETS
+#define BITNET_GEMM_EPI_SETS 4
+#endif
+constexpr int kGemmEpiSets = BITNET_GEMM_EPI_SETS;
 constexpr int kGemmEpiWarp2 = 12 + (kGemmDecSets - 1) * 4;  // first warp of epilogue set 1
 constexpr int kGemmThreads = 384 + (kGemmDecSets - 1) * 128 + (kGemmEpiSets - 1) * 128;
 constexpr int kGemmRows = 128;   // weight rows per tile (MMA M)
@@ -509,7 +512,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---------------------------------------------------------- epilogue --
     pdl_wait_prior_grid();
     const int quad = warp & 3, row = quad * 32 + lane;
-    const int eset = warp < 12 ? 0 : 1;  // which half of the token columns
+    const int eset = warp < 12 ? 0 : 1 + (warp - kGemmEpiWarp2) / 4;  // which share of the columns
     long long tc = 0;
     for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x, ++tc) {
       const int rt = (int)(t % p.NRT), tt = (int)(t / p.NRT);
@@ -519,7 +522,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const int64_t n = (int64_t)rt * kGemmRows + row;
 #pragma unroll 1
-      for (int cb = eset * (kGemmTok / 64); cb < (eset + 1) * (kGemmTok / 64); ++cb) {
+      for (int cb = eset * (kGemmTok / 32) / kGemmEpiSets; cb < (eset + 1) * (kGemmTok / 32) / kGemmEpiSets; ++cb) {
         // lane j fetches token tok0 + j's sum and scale (one coalesced load
         // each, issued before the TMEM load); the outputs take them by
         // shuffles, so no load waits behind an output store
