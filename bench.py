@@ -33,6 +33,12 @@ PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 
+# DRAM bytes (read + write) per launch of the dominant kernel, averaged over a
+# step, from one ncu capture of this kernel version (the launch list in
+# profiles/launches_2b_decode_fused_step.md); a step of another shape or
+# another kernel version reports null instead.
+MEASURED_TRAFFIC = {("2b-decode", 1, True, 0): 3.360e6}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -342,7 +348,9 @@ def run_native(args):
                    "l2": "inputs larger than L2 (packed stack %.0f MB > 126 MB L2)" % (wbytes / 1e6),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "frac": round(achieved / hbm_peak, 4),
+                     "traffic": MEASURED_TRAFFIC.get((args.workload, M, fused, G)),
+                     "algorithmic_bytes_per_launch": round(gemv_bytes / len(stack)),
                      "kernel": kname, "peak_source": peak_src,
                      "launches_timed": gemv_launches, "avg_launch_us": round(1e3 * gemv_ms / gemv_launches, 3)},
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
