@@ -181,6 +181,19 @@ def build_stack(args, dev, rank):
     return wl, stack, M
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum over the ranks of per-rank floats (the slowest
+    rank's times); the values themselves on one rank."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def init_dist():
     import torch
     import torch.distributed as dist
@@ -321,9 +334,7 @@ def run_native(args):
 
     ms_step = ms_total / args.steps
     if world > 1:  # max over ranks
-        t = torch.tensor([ms_step, e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, e2e_s = t[0].item(), t[1].item()
+        ms_step, e2e_s = max_over_ranks([ms_step, e2e_s], dev)
     value = world * wbytes / (ms_step * 1e-3) / 1e9
     e2e_val = world * wbytes * args.steps / e2e_s / 1e9
     achieved = gemv_bytes * n_meas / (gemv_ms * 1e-3) / 1e9
@@ -489,9 +500,7 @@ def run_ffn(args, dev, rank, world, hbm_peak, peak_src):
 
     ms_step = ms_total / args.steps
     if world > 1:
-        t = torch.tensor([ms_step, e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, e2e_s = t[0].item(), t[1].item()
+        ms_step, e2e_s = max_over_ranks([ms_step, e2e_s], dev)
     value = world * wbytes / (ms_step * 1e-3) / 1e9
     achieved = swiglu_bytes * args.layers * n_meas / (sw_ms * 1e-3) / 1e9
     down_bytes = dn.N * dn.K // 4 + 4 * M * I + 4 + 4 * M * D
@@ -618,9 +627,7 @@ def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
         e2e_s = (time.perf_counter() - t0) / args.steps
     tw.check_device_error(stream)
     if world > 1:
-        t = torch.tensor([ms_step, e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, e2e_s = t[0].item(), t[1].item()
+        ms_step, e2e_s = max_over_ranks([ms_step, e2e_s], dev)
     value = world * flops / (ms_step * 1e-3) / 1e12
     achieved = flops / (ms_gemm * 1e-3) / 1e12
     line = {

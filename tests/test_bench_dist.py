@@ -1,0 +1,63 @@
+"""The multi-rank host logic of bench.py, on CPU with the gloo backend and two
+ranks: the timing reduction takes the slowest rank's values, and the
+reference arm prints on rank 0 only (other ranks exit 0 without work)."""
+import os
+import socket
+import subprocess
+import sys
+
+from conftest import ROOT
+
+_RANK_CODE = r"""
+import os, sys, json
+sys.path.insert(0, os.environ["BENCH_ROOT"])
+import torch.distributed as dist
+dist.init_process_group("gloo")
+import bench
+rank = dist.get_rank()
+out = bench.max_over_ranks([1.0 + rank, 5.0 - rank, 3.0], "cpu")
+print(json.dumps({"rank": rank, "out": out}), flush=True)
+dist.barrier()
+dist.destroy_process_group()
+"""
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    import json
+
+    port = _free_port()
+    procs = []
+    for rank in range(2):
+        env = dict(os.environ, RANK=str(rank), WORLD_SIZE="2", LOCAL_RANK=str(rank), MASTER_ADDR="127.0.0.1",
+                   MASTER_PORT=str(port), BENCH_ROOT=ROOT)
+        procs.append(subprocess.Popen([sys.executable, "-c", _RANK_CODE], env=env, stdout=subprocess.PIPE,
+                                      stderr=subprocess.PIPE))
+    outs = []
+    for p in procs:
+        so, se = p.communicate(timeout=120)
+        assert p.returncode == 0, se.decode()[-2000:]
+        outs.append(json.loads(so.decode().strip().splitlines()[-1]))
+    for o in outs:
+        assert o["out"] == [2.0, 5.0, 3.0]
+    assert sorted(o["rank"] for o in outs) == [0, 1]
+
+
+def test_max_over_ranks_single_process():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.max_over_ranks([1.5, 2.5], "cpu") == [1.5, 2.5]
+
+
+def test_reference_arm_prints_on_rank_zero_only():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], cwd=ROOT, env=env, capture_output=True, timeout=300)
+    assert r.returncode == 0, r.stderr.decode()[-2000:]
+    assert r.stdout.strip() == b""
