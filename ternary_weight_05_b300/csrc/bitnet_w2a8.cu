@@ -420,7 +420,25 @@ bitnet_status static_scratch_address(void **out) {
 }
 
 bitnet_status launch_gemm_tc(uint32_t *xb, int32_t *xsum, float *fscale, int64_t M, const uint8_t *packed, int64_t N,
-                             int64_t K, float *y, int32_t *acc, const DeviceInfo *d, cudaStream_t stream);
+                             int64_t K, float *y, int32_t *acc, const GemmSplit &sp, uint8_t *part,
+                             const DeviceInfo *d, cudaStream_t stream);
+
+// Stream-K split of the GEMM's tail tiles when the workspace holds its
+// partial sums (sized for 148 SMs), else whole tiles only.
+GemmSplit gemm_plan_split(int64_t M, int64_t N, int64_t K, size_t ws_bytes, const DeviceInfo *d) {
+  GemmSplit sp = gemm_split(M, N, d->sms);
+  if (gemm_part_offset(M, K) + sp.part_bytes > ws_bytes) {
+    sp.tail = 0;
+    sp.full_tiles = sp.tiles;
+    sp.part_bytes = 0;
+  }
+  return sp;
+}
+
+// Prep CTAs that zero the split tail's partial sums and tickets (32 KB each).
+unsigned gemm_zero_ctas(const GemmSplit &sp) {
+  return sp.part_bytes ? (unsigned)std::min<int64_t>(148, cdiv((int64_t)sp.part_bytes, 32768)) : 0u;
+}
 
 }  // namespace
 
@@ -611,10 +629,13 @@ int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uin
   int32_t *xsum = reinterpret_cast<int32_t *>(ws + gemm_xb_bytes(M, K));
   float *fscale = reinterpret_cast<float *>(ws + gemm_xb_bytes(M, K) + (size_t)M * 4);
 
-  bitnet_status st = launch(gemm_prep_kernel, dim3((unsigned)M), dim3(256), 0, stream, x_q, scale, w_scale, K,
-                            xb, xsum, fscale, M, static_cast<uint4 *>(nullptr), (int64_t)0, 0);
+  const GemmSplit sp = gemm_plan_split(M, N, K, workspace_bytes, d);
+  uint8_t *part = ws + gemm_part_offset(M, K);
+  bitnet_status st = launch(gemm_prep_kernel, dim3((unsigned)M + gemm_zero_ctas(sp)), dim3(256), 0, stream, x_q,
+                            scale, w_scale, K, xb, xsum, fscale, M, reinterpret_cast<uint4 *>(part),
+                            (int64_t)(sp.part_bytes / 16), 0);
   if (st) return st;
-  return launch_gemm_tc(xb, xsum, fscale, M, packed, N, K, y, acc, d, stream);
+  return launch_gemm_tc(xb, xsum, fscale, M, packed, N, K, y, acc, sp, part, d, stream);
 }
 
 }  // extern "C"
@@ -623,7 +644,8 @@ namespace {
 
 // Main prefill GEMM launch; the prepared activations are at xb (workspace).
 bitnet_status launch_gemm_tc(uint32_t *xb, int32_t *xsum, float *fscale, int64_t M, const uint8_t *packed, int64_t N,
-                             int64_t K, float *y, int32_t *acc, const DeviceInfo *d, cudaStream_t stream) {
+                             int64_t K, float *y, int32_t *acc, const GemmSplit &sp, uint8_t *part,
+                             const DeviceInfo *d, cudaStream_t stream) {
   CUtensorMap wmap, bmap;
   if (bitnet_status s = encode_packed_map(&wmap, packed, N, K, 128, kGemmRows, CU_TENSOR_MAP_SWIZZLE_128B)) return s;
   {
@@ -648,6 +670,9 @@ bitnet_status launch_gemm_tc(uint32_t *xb, int32_t *xsum, float *fscale, int64_t
   p.NTT = (int)cdiv(M, kGemmTok);
   p.NKB = (int)cdiv(K, kGemmKB);
   p.tiles = (long long)p.NRT * p.NTT;
+  p.full_tiles = sp.tail ? sp.full_tiles : p.tiles;
+  p.ws_part = sp.tail ? reinterpret_cast<int32_t *>(part) : nullptr;
+  p.ws_ticket = sp.tail ? reinterpret_cast<unsigned *>(part + (size_t)sp.tail * kGemmTok * kGemmRows * 4) : nullptr;
   const size_t smem = gemm_smem_layout().bytes + 1024;
   if (set_smem(gemm_tc_kernel, smem) != BITNET_OK) return BITNET_ERR_CUDA;
   const int grid = (int)std::min<long long>(d->sms, p.tiles);
@@ -737,9 +762,11 @@ int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed,
     }
     fscale = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(xsum) + (size_t)M * 4);
     const bool gemv = M <= BITNET_GEMV_MAX_M;
-    const dim3 pgrid = gemv ? dim3(prep_grid(M, pl)) : dim3((unsigned)M);
-    uint4 *zero = gemv ? static_cast<uint4 *>(workspace) : nullptr;
-    const int64_t zero_n16 = gemv ? (int64_t)(pl.ws_zero_bytes / 16) : 0;
+    const GemmSplit sp = gemv ? GemmSplit{} : gemm_plan_split(M, N, K, workspace_bytes, d);
+    uint8_t *part = ws + gemm_part_offset(M, K);
+    const dim3 pgrid = gemv ? dim3(prep_grid(M, pl)) : dim3((unsigned)M + gemm_zero_ctas(sp));
+    uint4 *zero = gemv ? static_cast<uint4 *>(workspace) : reinterpret_cast<uint4 *>(part);
+    const int64_t zero_n16 = gemv ? (int64_t)(pl.ws_zero_bytes / 16) : (int64_t)(sp.part_bytes / 16);
     const int trows = gemv ? gemv_mma_rows(M) : 0;
     bitnet_status st =
         bf ? launch(fused_prep_kernel<__nv_bfloat16>, pgrid, dim3(256), 0, stream,
@@ -750,7 +777,7 @@ int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed,
     if (st) return st;
     if (M <= BITNET_GEMV_MAX_M)
       return launch_gemv_mma(nullptr, nullptr, M, packed, w_scale, N, K, y, acc, workspace, pl, d, stream);
-    return launch_gemm_tc(xb, xsum, fscale, M, packed, N, K, y, acc, d, stream);
+    return launch_gemm_tc(xb, xsum, fscale, M, packed, N, K, y, acc, sp, part, d, stream);
   }
   // Unfused: quantise into the caller's buffers or the workspace tail, then
   // the GEMV / GEMM entry points.

@@ -20,6 +20,12 @@
 //     D * 2^24 - sum_k x_q is the exact integer accumulator.
 //   * Two accumulators (256 TMEM columns) let the epilogue of one tile overlap
 //     the MMAs of the next.
+//   * When the tiles leave a last wave less than half full, those tail tiles
+//     are split by K across all CTAs (stream-K on the tail): after its whole
+//     tiles each CTA takes an equal run of (tail tile, 64-K block) units; the
+//     partial sums are added as exact int32 (D * 2^24) into the workspace,
+//     and the epilogue warp whose ticket completes a 32-row x (tokens / 4)
+//     block writes its outputs and re-zeroes the partials.
 // Warp roles: 0 TMA producer, 1 TMEM owner + MMA issuer, 4-7 decoders (set
 // 0), 8-11 epilogue, 12-15 ... further decoder sets.  Decoder set d takes
 // the K-blocks c with c % kGemmDecSets == d, so several blocks are in
@@ -74,6 +80,45 @@ struct GemmParams {
   int64_t M, N, K;
   int NRT, NTT, NKB;
   long long tiles;
+  long long full_tiles;  // tiles [0, full_tiles) are taken whole, round robin
+  int32_t *ws_part;      // split tail tiles: [tail][tokens][128 rows] int32, zero on entry and exit
+  unsigned *ws_ticket;   // [tail][16] K-blocks done per epilogue block, zero on entry and exit
+};
+
+// One run of K-blocks [kb0, kb1) of tile t.
+struct GemmSeg {
+  long long t;
+  int kb0, kb1;
+};
+
+// The segments of this CTA, in order: whole tiles blockIdx.x, + gridDim.x, ...
+// below full_tiles; then its equal share of the (tail tile, K-block) units.
+struct GemmSegIter {
+  long long tf, u, u_end;
+  __device__ explicit GemmSegIter(const GemmParams &p) {
+    tf = blockIdx.x;
+    const long long units = (p.tiles - p.full_tiles) * p.NKB;
+    u = units * blockIdx.x / gridDim.x;
+    u_end = units * (blockIdx.x + 1) / gridDim.x;
+  }
+  __device__ bool next(const GemmParams &p, GemmSeg &s) {
+    if (tf < p.full_tiles) {
+      s.t = tf;
+      s.kb0 = 0;
+      s.kb1 = p.NKB;
+      tf += gridDim.x;
+      return true;
+    }
+    if (u < u_end) {
+      const long long tl = u / p.NKB;
+      s.t = p.full_tiles + tl;
+      s.kb0 = (int)(u % p.NKB);
+      s.kb1 = (int)min((long long)p.NKB, s.kb0 + (u_end - u));
+      u += s.kb1 - s.kb0;
+      return true;
+    }
+    return false;
+  }
 };
 
 struct GemmSmem {
@@ -388,10 +433,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint64_t pol_b = l2_policy_evict_last();
       long long c = 0, wc = 0;
       bool waited_prior = false;
-      for (long long t = blockIdx.x; t < p.tiles && !*abort_flag; t += gridDim.x) {
-        const int rt = (int)(t % p.NRT), tt = (int)(t / p.NRT);
-        for (int kb = 0; kb < p.NKB && !*abort_flag; ++kb, ++c) {
-          if ((kb & 7) == 0) {
+      GemmSegIter it(p);
+      GemmSeg sg;
+      while (!*abort_flag && it.next(p, sg)) {
+        const int rt = (int)(sg.t % p.NRT), tt = (int)(sg.t / p.NRT);
+        for (int kb = sg.kb0; kb < sg.kb1 && !*abort_flag; ++kb, ++c) {
+          if ((kb & 7) == 0 || kb == sg.kb0) {  // the 512-K weight block holding kb
             const int ws = (int)(wc % kGemmWStages);
             if (wc >= kGemmWStages) wait(&wempty[ws], (uint32_t)(((wc / kGemmWStages) - 1) & 1));
             if (*abort_flag) break;
@@ -428,12 +475,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t idesc = gemm_idesc(kGemmRows, kGemmTok);
       const uint32_t bbase = smem_u32(smem + L.bstage);
       long long c = 0, tc = 0;
-      for (long long t = blockIdx.x; t < p.tiles && !*abort_flag; t += gridDim.x, ++tc) {
+      GemmSegIter it(p);
+      GemmSeg sg;
+      for (; !*abort_flag && it.next(p, sg); ++tc) {
         const int a = (int)(tc % kGemmAccBufs);
         if (tc >= kGemmAccBufs) wait(&accempty[a], (uint32_t)(((tc / kGemmAccBufs) - 1) & 1));
         tc_fence_after();
         const uint32_t d_tmem = tmem + kGemmAccCol + a * kGemmTok;
-        for (int kb = 0; kb < p.NKB && !*abort_flag; ++kb, ++c) {
+        for (int kb = sg.kb0; kb < sg.kb1 && !*abort_flag; ++kb, ++c) {
           const int s = (int)(c % kGemmStages);
           const uint32_t par = (uint32_t)((c / kGemmStages) & 1);
           wait(&bfull[s], par);
@@ -444,7 +493,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t a_tmem = tmem + kGemmACol + s * 32;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_ts(d_tmem, a_tmem + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+            tc_mma_ts(d_tmem, a_tmem + kk * 8, bdesc + (uint64_t)(kk * 2), idesc, (kb != sg.kb0) || kk != 0);
           tc_commit(&kempty[s]);
         }
         tc_commit(&accfull[a]);
@@ -462,12 +511,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t wbase = smem_u32(smem + L.wstage);
     long long c = 0, wc = 0;
     bool stop = false;
-    for (long long t = blockIdx.x; t < p.tiles && !stop; t += gridDim.x) {
-      for (int kb = 0; kb < p.NKB; ++kb, ++c) {
+    GemmSegIter it(p);
+    GemmSeg sg;
+    while (!stop && it.next(p, sg)) {
+      for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++c) {
         const int ws = (int)(wc % kGemmWStages);
-        if ((kb & 7) == 0) wait(&wfull[ws], (uint32_t)((wc / kGemmWStages) & 1));
+        if ((kb & 7) == 0 || kb == sg.kb0) wait(&wfull[ws], (uint32_t)((wc / kGemmWStages) & 1));
         const int chunk = kb & 7;
-        const bool last_of_wstage = chunk == 7 || kb == p.NKB - 1;
+        const bool last_of_wstage = chunk == 7 || kb == sg.kb1 - 1;
         if ((int)(c % kGemmDecSets) != dset) {  // another set decodes this block
           if (__any_sync(0xffffffffu, *abort_flag)) {
             stop = true;
@@ -513,16 +564,69 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     pdl_wait_prior_grid();
     const int quad = warp & 3, row = quad * 32 + lane;
     const int eset = warp < 12 ? 0 : 1 + (warp - kGemmEpiWarp2) / 4;  // which share of the columns
+    const int cb_begin = eset * (kGemmTok / 32) / kGemmEpiSets, cb_end = (eset + 1) * (kGemmTok / 32) / kGemmEpiSets;
     long long tc = 0;
-    for (long long t = blockIdx.x; t < p.tiles; t += gridDim.x, ++tc) {
+    GemmSegIter it(p);
+    GemmSeg sg;
+    for (; it.next(p, sg); ++tc) {
+      const long long t = sg.t;
       const int rt = (int)(t % p.NRT), tt = (int)(t / p.NRT);
       const int a = (int)(tc % kGemmAccBufs);
       wait(&accfull[a], (uint32_t)((tc / kGemmAccBufs) & 1));
       if (__any_sync(0xffffffffu, *abort_flag)) break;  // tcgen05.ld is warp-collective
       tc_fence_after();
       const int64_t n = (int64_t)rt * kGemmRows + row;
+      if (sg.kb0 != 0 || sg.kb1 != p.NKB) {
+        // part of a split tail tile: add the exact partial sums (D * 2^24,
+        // integers) into the workspace; the warp whose ticket completes this
+        // block of 32 rows x (its token columns) writes the outputs
+        const long long tl = t - p.full_tiles;
+        int32_t *part = p.ws_part + (size_t)tl * kGemmTok * kGemmRows;  // [token column][row]
 #pragma unroll 1
-      for (int cb = eset * (kGemmTok / 32) / kGemmEpiSets; cb < (eset + 1) * (kGemmTok / 32) / kGemmEpiSets; ++cb) {
+        for (int cb = cb_begin; cb < cb_end; ++cb) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + kGemmAccCol + a * kGemmTok + cb * 32, r);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            atomicAdd(part + (size_t)(cb * 32 + j) * kGemmRows + row,
+                      __float2int_rn(__uint_as_float(r[j]) * 16777216.0f));
+        }
+        __threadfence();
+        __syncwarp();
+        unsigned old = 0;
+        if (lane == 0) old = atomicAdd(p.ws_ticket + tl * 16 + eset * 4 + quad, (unsigned)(sg.kb1 - sg.kb0));
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old + (unsigned)(sg.kb1 - sg.kb0) == (unsigned)p.NKB) {
+          __threadfence();
+#pragma unroll 1
+          for (int cb = cb_begin; cb < cb_end; ++cb) {
+            const int64_t tok0 = (int64_t)tt * kGemmTok + cb * 32;
+            const int32_t xs_l = tok0 + lane < p.M ? __ldg(p.xsum + tok0 + lane) : 0;
+            const float fs_l = tok0 + lane < p.M ? __ldg(p.fscale + tok0 + lane) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int32_t xs = __shfl_sync(0xffffffffu, xs_l, j);
+              const float fs = __shfl_sync(0xffffffffu, fs_l, j);
+              int32_t *pp = part + (size_t)(cb * 32 + j) * kGemmRows + row;
+              const int32_t total = __ldcg(pp);
+              *pp = 0;
+              const int64_t tok = tok0 + j;
+              if (n < p.N && tok < p.M) {
+                const int32_t v = total - xs;
+                if (p.acc) p.acc[tok * p.N + n] = v;
+                p.y[tok * p.N + n] = __fmul_rn((float)v, fs);
+              }
+            }
+          }
+          if (lane == 0) p.ws_ticket[tl * 16 + eset * 4 + quad] = 0u;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&accempty[a]);
+        continue;
+      }
+#pragma unroll 1
+      for (int cb = cb_begin; cb < cb_end; ++cb) {
         // lane j fetches token tok0 + j's sum and scale (one coalesced load
         // each, issued before the TMEM load); the outputs take them by
         // shuffles, so no load waits behind an output store
@@ -562,9 +666,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 inline size_t gemm_xb_bytes(int64_t M, int64_t K) { return (((size_t)M * (size_t)K * 2) + 1023) & ~(size_t)1023; }
 
-inline size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  (void)N;
+// Whole tiles and stream-K tail: the tail is split when the last wave of
+// whole tiles would be less than half full on `sms` CTAs.
+struct GemmSplit {
+  long long tiles, full_tiles, tail;
+  size_t part_bytes;  // partial sums + tickets of the tail tiles
+};
+inline GemmSplit gemm_split(int64_t M, int64_t N, int sms) {
+  GemmSplit s;
+  s.tiles = (long long)((N + kGemmRows - 1) / kGemmRows) * ((M + kGemmTok - 1) / kGemmTok);
+  const long long rem = s.tiles % sms;
+  s.tail = (s.tiles > sms && rem > 0 && 2 * rem < sms) ? rem : 0;
+  s.full_tiles = s.tiles - s.tail;
+  s.part_bytes = (((size_t)s.tail * kGemmTok * kGemmRows * 4 + (size_t)s.tail * 16 * 4) + 255) & ~(size_t)255;
+  return s;
+}
+
+// Workspace: prepared activations, per-token sums and scales, then the
+// stream-K partials (sized for the 148 SMs of a B300).
+inline size_t gemm_part_offset(int64_t M, int64_t K) {
   return gemm_xb_bytes(M, K) + (((size_t)M * 8 + 255) & ~(size_t)255) + 1024;
+}
+inline size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  return gemm_part_offset(M, K) + gemm_split(M, N, 148).part_bytes;
 }
 
 }  // namespace bitnet

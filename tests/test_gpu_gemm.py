@@ -39,6 +39,37 @@ def test_gemm_tensor_core_path(lib, oracle_mod, cuda_dev, M, N, K):
     gemm_case(lib, oracle_mod, cuda_dev, M, N, K, seed=M + 7 * N + 13 * K)
 
 
+# more tiles than SMs with a last wave under half full: the tail tiles are
+# split by K across all CTAs (stream-K) and summed in the workspace.  150
+# tiles (2 split, K = 1024: 32 units over 148 CTAs, most CTAs one 64-K block),
+# 160 tiles (12 split, K = 2560: segments crossing tile boundaries), ragged M
+# and N, and the extreme-magnitude accumulators through the split.
+@pytest.mark.parametrize("M,N,K", [(300, 9600, 1024), (512, 10240, 2560), (300, 9500, 1088)])
+def test_gemm_stream_k_tail(lib, oracle_mod, cuda_dev, M, N, K):
+    gemm_case(lib, oracle_mod, cuda_dev, M, N, K, seed=M + N + K)
+
+
+def test_gemm_stream_k_extreme_and_workspace_reuse(lib, oracle_mod, cuda_dev):
+    import torch
+
+    M, N, K = 300, 9600, 2048
+    ws = torch.full((lib.gemm_workspace_bytes(M, N, K),), 0xAB, dtype=torch.uint8, device=cuda_dev)
+    rng = np.random.default_rng(11)
+    q = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    q[: N // 2] = 1
+    packed = oracle_mod.pack_codes(q)
+    for rep in range(2):  # the workspace starts with garbage, then holds the previous call's leftovers
+        xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+        xq[: M // 3] = 127
+        s = (rng.random(M) * 5 + 0.01).astype(np.float32)
+        y, acc = lib.w2a8_gemm(to_dev(xq, cuda_dev), to_dev(s, cuda_dev), to_dev(packed, cuda_dev),
+                               to_dev(np.array([np.float32(0.5)]), cuda_dev), N, K, want_acc=True, workspace=ws)
+        acc_ref = oracle_mod.contract(xq, packed, N, K, threads=8)
+        assert np.array_equal(acc.cpu().numpy(), acc_ref), rep
+        assert_y_close(y.cpu().numpy(), oracle_mod.epilogue(acc_ref, s, 0.5))
+    lib.check_device_error()
+
+
 def test_gemm_extreme_accumulators(lib, oracle_mod, cuda_dev):
     # |acc| = 127 * K = 1,040,384 at K = 8192: the largest magnitude the fp32
     # accumulation must still hold exactly
