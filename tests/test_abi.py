@@ -206,6 +206,18 @@ def test_workspace_sizes_cover_partials(clib):
     assert clib.bitnet_gemm_workspace_bytes(2048, 6912, 2560) > 0
 
 
+def test_gemm_workspace_covers_the_split_tail(clib):
+    # 2048 tokens x 2560 rows: 8 x 20 = 160 tiles of 256 x 128 on 148 SMs,
+    # a last wave of 12 tiles whose K loops are split across the CTAs: the
+    # workspace holds their int32 partial sums (256 x 128 each) and tickets
+    xb = 2048 * 6912 * 2
+    split = clib.bitnet_gemm_workspace_bytes(2048, 2560, 6912)
+    assert split >= xb + 2048 * 8 + 12 * 256 * 128 * 4 + 12 * 16 * 4
+    # 2048 x 6912: 432 tiles, a last wave of 136 (over half full): no split
+    whole = clib.bitnet_gemm_workspace_bytes(2048, 6912, 2560)
+    assert whole == ((2048 * 2560 * 2 + 1023) // 1024) * 1024 + ((2048 * 8 + 255) // 256) * 256 + 1024
+
+
 def test_package_fails_loudly_without_library(tmp_path, monkeypatch):
     from ternary_weight_05_b300 import _lib
 
