@@ -261,10 +261,7 @@ bitnet_status launch_gemv_ldg(const int8_t *x_q, const float *scale, const void 
   p.K = K;
   p.M = (int)M;
   p.C = (int)(K / 64);
-#ifndef BITNET_LDG_GRID_MULT
-#define BITNET_LDG_GRID_MULT 1
-#endif
-  const int grid = (int)std::min<int64_t>((int64_t)d->sms * BITNET_LDG_GRID_MULT, cdiv(N, kLdgWarps));
+  const int grid = (int)std::min<int64_t>(d->sms, cdiv(N, kLdgWarps));
   // ring sized to the rows a warp owns: at most ceil(N / warps) rows
   // (SwiGLU: gate and up rows; grouped: the packed row and its scales)
   const int64_t rowb = (SW ? 2 : 1) * (K / 4) + (GR ? 4 * (K / G) : 0);

@@ -66,24 +66,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-#ifndef BITNET_WAIT_MODE
-#define BITNET_WAIT_MODE 0
-#endif
-
-__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Waits for the phase with the given parity to complete.  Returns false if
 // kWaitLimitNs elapses first (the caller then records the error and leaves).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-#if BITNET_WAIT_MODE == 0
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
@@ -92,19 +77,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
       if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
-#elif BITNET_WAIT_MODE == 1
-  // try_wait loop bounded by the SM clock (>= 1.5 s at up to 2.1 GHz)
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > 3200000000ll) return false;
-  return true;
-#else
-  // non-suspending spin bounded by the SM clock
-  const long long t0 = clock64();
-  while (!mbar_test_wait(bar, parity))
-    if (clock64() - t0 > 3200000000ll) return false;
-  return true;
-#endif
 }
 
 // -------------------------------------------------------------------- TMA --

@@ -52,9 +52,6 @@ namespace bitnet {
 #ifndef BITNET_LDG_WARPS
 #define BITNET_LDG_WARPS 12
 #endif
-#ifndef BITNET_LDG_MIN_CTAS
-#define BITNET_LDG_MIN_CTAS 1
-#endif
 constexpr int kLdgWarps = BITNET_LDG_WARPS;
 constexpr int kLdgThreads = kLdgWarps * 32;
 #ifndef BITNET_LDG_STAGE_BYTES
@@ -140,7 +137,7 @@ __host__ __device__ inline GemvLdgSmem gemv_ldg_smem_layout(int MT, int C, int R
 }
 
 template <int MT, int J, typename XT, int FORM>
-__global__ void __launch_bounds__(kLdgThreads, BITNET_LDG_MIN_CTAS) gemv_ldg_kernel(const GemvLdgParams p) {
+__global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgParams p) {
   constexpr bool SW = FORM == kLdgSwiGLU, GR = FORM == kLdgGrouped;
   extern __shared__ __align__(128) uint8_t lsm[];
   const GemvLdgSmem L = gemv_ldg_smem_layout(MT, p.C, p.RS, p.NS, GR ? p.NG : 0);

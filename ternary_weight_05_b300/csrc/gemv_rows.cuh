@@ -42,9 +42,6 @@ constexpr int kRowsStageBytes = kRowsGroup * 128;  // 8 KB
 #ifndef BITNET_ROWS_MAX_STAGES
 #define BITNET_ROWS_MAX_STAGES 24
 #endif
-#ifndef BITNET_ROWS_EARLY_PDL
-#define BITNET_ROWS_EARLY_PDL 1
-#endif
 constexpr int kRowsMaxStages = BITNET_ROWS_MAX_STAGES;
 constexpr int kRowsBar = 1;
 constexpr int kRowsXBudget = 96 * 1024;  // activation words in shared memory
@@ -147,7 +144,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
 
   // Dependents may launch now: they wait for this grid's completion before
   // reading anything it writes, and their weight prefetch can overlap it.
-  if (BITNET_ROWS_EARLY_PDL) pdl_launch_dependents();
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
@@ -200,7 +197,6 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
 
   // ---------------------------------------------------------- compute warps --
   pdl_wait_prior_grid();
-  if (!BITNET_ROWS_EARLY_PDL) pdl_launch_dependents();
   const int tid = threadIdx.x;
   // activation words: for 16-K group q, word s holds bytes x[16q + 4b + s]
   if (tid < MT) xsum[tid] = 0;
