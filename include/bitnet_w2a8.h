@@ -135,9 +135,15 @@ size_t bitnet_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 /*
  * bitnet_w2a8_gemm -- prefill-path ternary matmul (same operation and
  * arguments as bitnet_w2a8_gemv, any M >= 1; tuned for M >= 256) on the
- * tcgen05 tensor cores with TMEM accumulators.  Same citations as the GEMV.
- *   workspace device, >= bitnet_gemm_workspace_bytes(M, N, K) bytes, any
- *             contents (the GEMM keeps no state in it between calls).
+ * tcgen05 tensor cores with TMEM accumulators, 128 weight rows x 256 tokens
+ * per tile.  When the tiles leave a last wave less than half full, those
+ * tiles are split by K across all SMs and their exact int32 partial sums
+ * meet in the workspace.  Same citations as the GEMV.
+ *   workspace device, >= bitnet_gemm_workspace_bytes(M, N, K) bytes,
+ *             256-byte aligned, any contents (the call prepares what it
+ *             uses, in stream order; no state is kept between calls).
+ * Shapes outside the tensor-core path (K % 64 != 0, K < 512, K > 65536,
+ * unaligned pointers) run a plain CUDA-core kernel with the same results.
  */
 int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
                      const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc,
