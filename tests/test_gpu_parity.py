@@ -196,6 +196,29 @@ def test_matmul_beyond_fp32_exact_k(lib, oracle_mod, cuda_dev, fn, M):
     assert_y_close(y.cpu().numpy(), y_ref)
 
 
+@pytest.mark.parametrize("fn", ["gemv", "gemm"])
+@pytest.mark.parametrize("M", [1, 3, 20])
+def test_matmul_at_the_fp32_exact_limit(lib, oracle_mod, cuda_dev, fn, M):
+    # K = 65536, the longest row the tensor-core paths take: every weight +1
+    # and every activation 127 give sum code * x = 2 * 127 * 65536 =
+    # 16,646,144 < 2^24, still exact in the fp32 accumulators
+    N, K = 40, 65536
+    q = np.ones((N, K), dtype=np.int8)
+    q[1::2, ::7] = -1
+    packed = oracle_mod.pack_codes(q)
+    xq = np.full((M, K), 127, dtype=np.int8)
+    xq[-1, ::5] = -127
+    s = np.full(M, 2.0, dtype=np.float32)
+    acc_ref = oracle_mod.contract(xq, packed, N, K, threads=8)
+    assert acc_ref.max() == K * 127  # the extreme magnitude is reached
+    y_ref = oracle_mod.epilogue(acc_ref, s, 0.5)
+    f = lib.w2a8_gemv if fn == "gemv" else lib.w2a8_gemm
+    y, acc = f(to_dev(xq, cuda_dev), to_dev(s, cuda_dev), to_dev(packed, cuda_dev),
+               to_dev(np.array([0.5], np.float32), cuda_dev), N, K, want_acc=True)
+    assert np.array_equal(acc.cpu().numpy(), acc_ref)
+    assert_y_close(y.cpu().numpy(), y_ref)
+
+
 def test_gemv_workspace_any_contents(lib, oracle_mod, cuda_dev):
     # one workspace, filled with garbage, shared by calls of different shapes
     # and paths (tensor-core stream-K, row-range, mma.sync stream-K for
