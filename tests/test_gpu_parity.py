@@ -207,7 +207,8 @@ def test_matmul_at_the_fp32_exact_limit(lib, oracle_mod, cuda_dev, fn, M):
     q[1::2, ::7] = -1
     packed = oracle_mod.pack_codes(q)
     xq = np.full((M, K), 127, dtype=np.int8)
-    xq[-1, ::5] = -127
+    if M > 1:
+        xq[-1, ::5] = -127
     s = np.full(M, 2.0, dtype=np.float32)
     acc_ref = oracle_mod.contract(xq, packed, N, K, threads=8)
     assert acc_ref.max() == K * 127  # the extreme magnitude is reached
