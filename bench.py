@@ -39,6 +39,15 @@ FALLBACK_BF16_TFLOPS = 1800.0
 # another kernel version reports null instead.
 MEASURED_TRAFFIC = {("2b-decode", 1, True, 0): 3.360e6}
 
+# Output rows of each prefill matrix the CPU oracle computes per sample pass
+# (all 2048 tokens, the whole K), to keep its timing bounded.
+PREFILL_ORACLE_ROWS = 32
+
+
+def metric_unit(workload):
+    """(unit, divisor of the per-second amount) of the metric for a workload."""
+    return ("TOPS", 1e12) if workload == "prefill-2048" else ("GB/s", 1e9)
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -648,8 +657,7 @@ def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
         "clocks": clk,
     }
     if rank == 0:
-        line["cpu_baseline"] = {"value": None, "unit": "TOPS", "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": "not run for the prefill workload"}
+        line["cpu_baseline"] = cpu_baseline(args)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -660,7 +668,8 @@ def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
 
 def oracle_sample(args):
     """One layer of the workload for the oracle (bounded sample): a list of
-    (name, packed weight bytes, callable running the oracle on it)."""
+    (name, amount, callable running the oracle on it), the amount in the
+    metric's numerator (packed weight bytes; flops for the prefill GEMM)."""
     import numpy as np
 
     import oracle
@@ -671,6 +680,19 @@ def oracle_sample(args):
         packed, beta, _ = oracle.pack_weights(W)
         return packed, beta
 
+    if args.workload == "prefill-2048":
+        # every token, the first PREFILL_ORACLE_ROWS output rows of each matrix
+        wl = synth.workload("prefill-2048")
+        M = 2048
+        sample = []
+        for L in wl.layers:
+            packed, beta = host_packed(L)
+            _, x = synth.acts_np(M, L.K, L.x_dist, seed=L.x_seed, outlier_p=L.outlier_p, bf16=L.x_bf16)
+            R = PREFILL_ORACLE_ROWS
+            sample.append((f"{L.name}[:{R}]", 2 * M * R * L.K,
+                           lambda threads, L=L, p=packed[:R * L.K // 4], b=beta, x=x, R=R: oracle.bitlinear(
+                               x, p, b, R, L.K, threads=threads)))
+        return sample, M
     if args.workload == "ffn-2b-decode":
         wl = synth.workload("ffn-2b-decode")
         gu, dn = wl.layers
@@ -705,56 +727,58 @@ def oracle_sample(args):
     return sample, M
 
 
-def time_oracle(sample, seconds, threads):
-    done_bytes, t0, passes = 0, time.perf_counter(), 0
+def time_oracle(sample, seconds, threads, div=1e9):
+    done, t0, passes = 0, time.perf_counter(), 0
     while True:
-        for _, nbytes, fn in sample:
+        for _, amount, fn in sample:
             fn(threads)
-            done_bytes += nbytes
+            done += amount
         passes += 1
         el = time.perf_counter() - t0
         if el >= seconds:
-            return done_bytes / el / 1e9, el, passes
+            return done / el / div, el, passes
 
 
 def cpu_baseline(args):
+    unit, div = metric_unit(args.workload)
     try:
         sample, M = oracle_sample(args)
         cores = os.cpu_count() or 1
-        gbs, el, passes = time_oracle(sample, args.cpu_seconds, cores)
+        v, el, passes = time_oracle(sample, args.cpu_seconds, cores, div)
         names = ",".join(name for name, *_ in sample)
-        return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+        return {"value": round(v, 4), "unit": unit, "cores": cores, "kind": "oracle",
                 "sample": f"{passes} pass(es) over one layer ({names}; M={M}) in {el:.1f} s, "
                           f"rows split over {cores} threads"}
     except Exception as ex:  # the baseline must never break the GPU line
-        return {"value": None, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle", "sample": f"failed: {ex}"}
+        return {"value": None, "unit": unit, "cores": os.cpu_count(), "kind": "oracle", "sample": f"failed: {ex}"}
 
 
 def run_reference(args):
     if int(os.environ.get("RANK", "0")) != 0:
         return
     sample, M = oracle_sample(args)
+    unit, div = metric_unit(args.workload)
     cores = os.cpu_count() or 1
     per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        time_oracle(sample, per_step / 4, cores)
+        time_oracle(sample, per_step / 4, cores, div)
     vals = []
     for _ in range(args.steps):
-        gbs, _, _ = time_oracle(sample, per_step, cores)
-        vals.append(gbs)
+        v, _, _ = time_oracle(sample, per_step, cores, div)
+        vals.append(v)
     value = statistics.median(vals)
-    wbytes = sum(nbytes for _, nbytes, _ in sample)
+    amount = sum(a for _, a, _ in sample)
     names = ",".join(name for name, *_ in sample)
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * wbytes / (value * 1e9), 3),
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * amount / (value * div), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
         "data": "synthetic (seeded numpy PCG64)",
         "config": {"workload": args.workload, "M": M, "sample": f"one layer ({names}) per step"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": f"each step: >= {per_step:.1f} s of passes over one layer ({names}), "
                                    f"rows split over {cores} threads"},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
