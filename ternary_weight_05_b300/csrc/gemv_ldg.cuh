@@ -1,4 +1,4 @@
-// Decode GEMV for one or two tokens streamed with plain coalesced loads.
+// Decode GEMV for one or two tokens: warp-private bulk-copy streams.
 //
 // Same operation as the other GEMV kernels (BitNet 深度拆解 §3.1 integer-
 // domain product, §1 ternary products, §2.3 dequantisation).  This is the
@@ -6,9 +6,10 @@
 // weights, organised so that nothing serialises the weight stream:
 //   * Every warp owns a contiguous range of whole rows, i.e. a contiguous
 //     byte range of the packed matrix, and streams it through a private ring
-//     of two 8 KB shared-memory stages with 1D bulk copies (cp.async.bulk):
-//     up to 192 KB in flight per SM, no coupling between warps, no barrier
-//     but the warp's own stage barriers.  The first stages are requested
+//     of up to two 8 KB shared-memory stages (sized to the rows the warp
+//     owns, so small matrices leave the SM's shared memory free) with 1D bulk
+//     copies (cp.async.bulk): up to 192 KB in flight per SM, no coupling
+//     between warps, no barrier but the warp's own stage barriers.  The first stages are requested
 //     before waiting on the previous kernel, since the weights do not depend
 //     on it.  Lane l reads the 16-byte chunks l, l+32, ... of each row from
 //     the stage (consecutive lanes, consecutive addresses: conflict-free).
@@ -17,11 +18,14 @@
 //     x_q[16q + 4b + s], b = 0..3, so masking a packed word with
 //     0x03030303 << 2s and dp4a against word s gives 4^s * sum code * x
 //     (2 integer operations per packed byte per token).
-//   * A row's 32 lane sums are combined with warp shuffles; lane 0 subtracts
-//     the token's sum of x_q and applies the fused dequantisation.
+//   * A row's 32 lane sums are combined with warp shuffles; lane m subtracts
+//     token m's sum of x_q and applies the fused dequantisation.
 //   * Fused form (XT = float / bf16): the CTA quantises x itself in its
 //     prologue (absmax, then clamp(rint(x / s * 127)), the operations of
-//     quant_act_kernel), so one kernel runs the whole BitLinear.
+//     quant_act_kernel, on 8-element halves of 16-K groups spread over all
+//     threads), so one kernel runs the whole BitLinear.  The activation words
+//     sit in shared memory in a lane-consecutive order before the lanes load
+//     theirs.
 //   * SwiGLU form (SW): the front half of the BitTransformer feed-forward of
 //     BitNet 深度拆解 §3.1, silu(gate(h)) * up(h).  A stage holds gate rows
 //     and the up rows of the same indices (two bulk copies); both sums are
