@@ -1,6 +1,5 @@
 """The C-ABI library loads, exports every declared symbol and rejects bad
 arguments on the host before touching the GPU (no GPU needed)."""
-import ctypes
 import glob
 import os
 import re
