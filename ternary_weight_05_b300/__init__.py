@@ -53,22 +53,29 @@ def _dev(t: torch.Tensor, name: str):
 
 
 def pack_workspace_bytes(N: int, K: int) -> int:
+    """Bytes of device scratch pack_weights needs for an [N, K] matrix."""
     return int(_L().bitnet_pack_workspace_bytes(N, K))
 
 
 def gemv_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Bytes of device scratch w2a8_gemv needs (M <= 64 tokens, N x K weights)."""
     return int(_L().bitnet_gemv_workspace_bytes(M, N, K))
 
 
 def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Bytes of device scratch w2a8_gemm needs (M tokens, N x K weights)."""
     return int(_L().bitnet_gemm_workspace_bytes(M, N, K))
 
 
 def set_pdl(enable: bool) -> None:
+    """Launch this thread's kernels with programmatic dependent launch (each
+    kernel still waits for its predecessor before touching its outputs)."""
     _L().bitnet_set_pdl(1 if enable else 0)
 
 
 def check_device_error(stream=None) -> None:
+    """Synchronise `stream` (default: the current one) and raise if a kernel's
+    bounded wait expired since the last check."""
     s = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream
     _lib.check("bitnet_check_device_error", _L().bitnet_check_device_error(s))
 
@@ -184,6 +191,7 @@ def w2a8_gemv_static_scratch(x_q, scale, packed, w_scale, N: int, K: int, want_a
 
 
 def bitlinear_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Bytes of device scratch bitlinear needs."""
     return int(_L().bitnet_bitlinear_workspace_bytes(M, N, K))
 
 
@@ -222,6 +230,7 @@ def bitlinear(x: torch.Tensor, packed: torch.Tensor, w_scale: torch.Tensor, N: i
 
 
 def bitlinear_swiglu_workspace_bytes(M: int, I: int, K: int) -> int:
+    """Bytes of device scratch bitlinear_swiglu needs (I rows in each of gate and up)."""
     return int(_L().bitnet_bitlinear_swiglu_workspace_bytes(M, I, K))
 
 
@@ -333,6 +342,7 @@ def bitlinear_grouped(x: torch.Tensor, packed: torch.Tensor, w_scale: torch.Tens
 
 
 def bitlinear_grouped_workspace_bytes(M: int, K: int) -> int:
+    """Bytes of device scratch bitlinear_grouped needs."""
     return int(_L().bitnet_bitlinear_grouped_workspace_bytes(M, K))
 
 
@@ -374,4 +384,5 @@ def bitlinear_fake_quant(W: torch.Tensor, x: torch.Tensor, weight_scale=None, al
 
 
 def bitlinear_fake_quant_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Bytes of device scratch bitlinear_fake_quant needs (the packed copy of W included)."""
     return int(_L().bitnet_bitlinear_fake_quant_workspace_bytes(M, N, K))
