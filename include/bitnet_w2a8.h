@@ -348,6 +348,17 @@ int bitnet_w2a8_gemv_static_scratch(const int8_t *x_q, const float *scale, int64
                                     int64_t K, float *y, int32_t *acc, cudaStream_t stream);
 
 /*
+ * bitnet_selftest_wait_timeout -- exercises the failure path without a
+ * fault: one kernel waits on an on-chip barrier that nothing completes,
+ * gives up after limit_ns (1 us .. 1 s) of wall-clock time, records the
+ * timeout in the device error word exactly as a stuck pipeline stage would,
+ * and returns; the next bitnet_check_device_error reports
+ * BITNET_ERR_TIMEOUT and the context stays usable.
+ * Errors: INVALID_ARG (limit out of range), UNSUPPORTED, CUDA.
+ */
+int bitnet_selftest_wait_timeout(int64_t limit_ns, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word of the
  * current device.  Returns BITNET_OK, BITNET_ERR_TIMEOUT (a kernel's bounded
  * wait expired since the last check) or BITNET_ERR_CUDA.

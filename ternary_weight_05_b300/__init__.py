@@ -386,3 +386,11 @@ def bitlinear_fake_quant(W: torch.Tensor, x: torch.Tensor, weight_scale=None, al
 def bitlinear_fake_quant_workspace_bytes(M: int, N: int, K: int) -> int:
     """Bytes of device scratch bitlinear_fake_quant needs (the packed copy of W included)."""
     return int(_L().bitnet_bitlinear_fake_quant_workspace_bytes(M, N, K))
+
+
+def selftest_wait_timeout(limit_ns: int = 2_000_000, stream=None) -> None:
+    """Run the failure-path self-test: a kernel whose bounded on-chip wait
+    expires after limit_ns records a timeout in the device error word (the
+    next check_device_error raises BitnetError TIMEOUT)."""
+    s = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    _lib.check("bitnet_selftest_wait_timeout", _L().bitnet_selftest_wait_timeout(int(limit_ns), s))

@@ -971,6 +971,13 @@ int bitnet_bitlinear_fake_quant(const void *W, int w_dtype, const void *x, int x
   return bitnet_bitlinear(x, x_dtype, M, pk, bt, N, K, y, x_q, scale, acc, tail, tail_bytes, stream);
 }
 
+int bitnet_selftest_wait_timeout(int64_t limit_ns, cudaStream_t stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000) return BITNET_ERR_INVALID_ARG;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
+  return launch(selftest_wait_kernel, dim3(1), dim3(32), 0, stream, (unsigned long long)limit_ns);
+}
+
 int bitnet_check_device_error(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return BITNET_ERR_CUDA;
   unsigned v = 0, zero = 0;

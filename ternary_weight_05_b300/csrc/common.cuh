@@ -167,4 +167,24 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
 __device__ __forceinline__ float load_as_f32(const float *p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float load_as_f32(const __nv_bfloat16 *p, int64_t i) { return __bfloat162float(p[i]); }
 
+// Failure-path self-test: one thread waits on a barrier that nothing
+// completes, with the same bounded loop as mbar_wait but a caller-chosen
+// limit, then records the timeout like a stuck pipeline would and returns.
+__global__ void selftest_wait_kernel(unsigned long long limit_ns) {
+  pdl_wait_prior_grid();  // keeps completion transitive along the stream
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(&bar, 0))
+    if (global_timer_ns() - t0 > limit_ns) {
+      raise_device_error(kDevErrTimeout);
+      return;
+    }
+}
+
 }  // namespace bitnet

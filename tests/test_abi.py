@@ -217,6 +217,11 @@ def test_gemm_workspace_covers_the_split_tail(clib):
     assert whole == ((2048 * 2560 * 2 + 1023) // 1024) * 1024 + ((2048 * 8 + 255) // 256) * 256 + 1024
 
 
+def test_selftest_wait_validation(clib):
+    assert clib.bitnet_selftest_wait_timeout(10, None) == INVALID_ARG          # below 1 us
+    assert clib.bitnet_selftest_wait_timeout(2_000_000_000, None) == INVALID_ARG  # above 1 s
+
+
 def test_package_fails_loudly_without_library(tmp_path, monkeypatch):
     from ternary_weight_05_b300 import _lib
 
