@@ -54,6 +54,9 @@ def _load():
         "oracle_pack_weights_grouped": (None, [_p, _i64, _i64, _i64, _f32, _f32, _p, _p, _p]),
         "oracle_contract_grouped": (None, [_p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
         "oracle_epilogue_grouped": (None, [_p, _p, _p, _i64, _i64, _i64, _p, _p]),
+        "oracle_sum_squares": (ctypes.c_double, [_p, _i64]),
+        "oracle_rmsnorm_apply": (None, [_p, _p, _i64, _f32, _f32, _p, _p]),
+        "oracle_rmsnorm": (None, [_p, _p, _i64, _i64, _f32, _p, _p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -286,3 +289,53 @@ def bitlinear_fake_quant(W: np.ndarray, x: np.ndarray, weight_scale=None, alpha:
     ws = np.ascontiguousarray(weight_scale, dtype=np.float32).reshape(N, 1)
     y, cond, acc_g, xq, s = bitlinear_grouped(x, packed, ws, N, K, K, threads=threads)
     return y, cond, acc_g[:, :, 0], xq, s, packed, beta
+
+
+# nn.RMSNorm's default eps for fp32 inputs: the machine epsilon of fp32
+RMS_EPS = 2.0 ** -23
+
+
+def sum_squares(x: np.ndarray) -> float:
+    """S = sum x_k^2 of one token, fp64, left to right."""
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    return float(_load().oracle_sum_squares(_ptr(x), x.size))
+
+
+def rmsnorm(x: np.ndarray, g=None, eps: float = RMS_EPS):
+    """RMSNorm per token of x fp32 [M, K] with weight g [K] (None = ones):
+    returns (h fp32 [M, K], ms fp32 [M], the mean squares)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.ndim == 2
+    M, K = x.shape
+    h = np.empty((M, K), dtype=np.float32)
+    ms = np.empty(M, dtype=np.float32)
+    gp = None
+    if g is not None:
+        g = np.ascontiguousarray(g, dtype=np.float32).ravel()
+        assert g.size == K
+        gp = _ptr(g)
+    _load().oracle_rmsnorm(_ptr(x), gp, M, K, eps, _ptr(h), _ptr(ms))
+    return h, ms
+
+
+def rmsnorm_apply(x_row: np.ndarray, ms: float, g=None, eps: float = RMS_EPS):
+    """One token normalised with a given fp32 mean square: (h [K], r)."""
+    x_row = np.ascontiguousarray(x_row, dtype=np.float32).ravel()
+    K = x_row.size
+    h = np.empty(K, dtype=np.float32)
+    r = np.zeros(1, dtype=np.float32)
+    gp = None
+    if g is not None:
+        g = np.ascontiguousarray(g, dtype=np.float32).ravel()
+        assert g.size == K
+        gp = _ptr(g)
+    _load().oracle_rmsnorm_apply(_ptr(x_row), gp, K, np.float32(ms), eps, _ptr(h), _ptr(r))
+    return h, np.float32(r[0])
+
+
+def bitlinear_rmsnorm(x: np.ndarray, g, packed: np.ndarray, beta: float, N: int, K: int, eps: float = RMS_EPS,
+                      threads: int = 1):
+    """RMSNorm, then the BitLinear forward: returns (y, acc, xq, s, h, ms)."""
+    h, ms = rmsnorm(x, g, eps)
+    y, acc, xq, s = bitlinear(h, packed, beta, N, K, threads=threads)
+    return y, acc, xq, s, h, ms

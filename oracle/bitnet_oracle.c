@@ -266,3 +266,42 @@ void oracle_epilogue_grouped(const int32_t *acc_g, const float *scale, const flo
       cond[m * N + n] = c * (double)scale[m] / 127.0;
     }
 }
+
+/* RMSNorm in front of a BitLinear (the feed-forward input of the
+ * BitTransformer block, [Deep-dive] section 3.1: h = norm2(x), then gate(h)
+ * and up(h); norms stay fp32, same section and section 6.5).  nn.RMSNorm
+ * computes h_k = x_k / sqrt(mean_k(x_k^2) + eps) * g_k per token.  Readings:
+ *   - the sum of squares S is formed in fp64, left to right (the square of an
+ *     fp32 value is exact in fp64); ms = (float)(S / K);
+ *   - t = ms + eps and the inverse rms r = 1 / sqrt(t) are three fp32 IEEE
+ *     operations (add, sqrt, division), the division once per token;
+ *   - h_k = (x_k * r) * g_k, two fp32 products; g = NULL means the module's
+ *     initial weight, all ones, and the second product is skipped (x * 1).
+ * The absmax quantisation of section 2.2 then runs on h. */
+double oracle_sum_squares(const float *x, int64_t K) {
+  double s = 0.0;
+  for (int64_t k = 0; k < K; k++) s += (double)x[k] * (double)x[k];
+  return s;
+}
+
+/* One token: h = (x * r) * g from a given mean square ms. */
+void oracle_rmsnorm_apply(const float *x, const float *g, int64_t K, float ms, float eps, float *h, float *r_out) {
+  float t = ms + eps;
+  float rms = sqrtf(t);
+  float r = 1.0f / rms;
+  for (int64_t k = 0; k < K; k++) {
+    float v = x[k] * r;
+    h[k] = g ? v * g[k] : v;
+  }
+  if (r_out) *r_out = r;
+}
+
+/* x, h [M, K] row-major; g [K] or NULL; ms [M] receives each token's mean
+ * square (fp32). */
+void oracle_rmsnorm(const float *x, const float *g, int64_t M, int64_t K, float eps, float *h, float *ms) {
+  for (int64_t m = 0; m < M; m++) {
+    float msq = (float)(oracle_sum_squares(x + m * K, K) / (double)K);
+    ms[m] = msq;
+    oracle_rmsnorm_apply(x + m * K, g, K, msq, eps, h + m * K, 0);
+  }
+}

@@ -513,3 +513,124 @@ def test_fake_quant_forward_matches_page_torch_module(oracle_mod, learned):
         assert np.all(cond >= np.abs(y) * (1 - 1e-12))
     else:
         np.testing.assert_allclose(y, ref.float().numpy(), rtol=3e-7, atol=0)
+
+
+# ----------------------------------------- RMSNorm in front of a BitLinear --
+
+def test_rmsnorm_worked_examples(oracle_mod):
+    # [3, 4, 0, 0]: mean square 25/4, rms 5/2, h = [6/5, 8/5, 0, 0].  Constant
+    # rows normalise to 1: a LayerNorm (x - mean) would give 0, a sum instead
+    # of a mean 1/2, a missing square root 1/c.  (In every row eps = 2^-23 is
+    # below half an ulp of the mean square, so t = ms.)  The weight multiplies
+    # element by element.
+    x = np.array([[3, 4, 0, 0], [2, 2, 2, 2], [-5, -5, -5, -5], [6, 6, 6, 6]], np.float32)
+    h, ms = oracle_mod.rmsnorm(x)
+    assert ms.tolist() == [6.25, 4.0, 25.0, 36.0]
+    assert h[0].tolist() == np.array([1.2, 1.6, 0, 0], np.float32).tolist()
+    assert h[1:].tolist() == [[1.0] * 4, [-1.0] * 4, [1.0] * 4]
+    g = np.array([1, -2, 0.5, 4], np.float32)
+    hg, _ = oracle_mod.rmsnorm(x, g)
+    assert hg[1:].tolist() == [g.tolist(), (-g).tolist(), g.tolist()]
+
+
+def test_rmsnorm_eps_enters_under_the_root(oracle_mod):
+    # A constant row c = 2^-12: c^2 = 2^-24, t = 2^-24 + 2^-23 = 3 * 2^-24, so
+    # h = c / sqrt(3 c^2) = 1/sqrt(3).  eps added to the rms instead would give
+    # ~0.9995, a dropped eps 1.
+    c = 2.0 ** -12
+    h, ms = oracle_mod.rmsnorm(np.full((1, 64), c, np.float32))
+    assert ms[0] == np.float32(2.0 ** -24)
+    assert np.allclose(h, 1.0 / math.sqrt(3.0), rtol=4 * 2.0 ** -24, atol=0)
+    # a zero row stays zero (t = eps > 0): no NaN
+    h0, ms0 = oracle_mod.rmsnorm(np.zeros((1, 16), np.float32))
+    assert ms0[0] == 0.0 and np.all(h0 == 0.0)
+
+
+@pytest.mark.parametrize("sigma", [1e-2, 1.0, 300.0])
+def test_rmsnorm_output_has_unit_rms(oracle_mod, sigma):
+    # mean_k h_k^2 = ms / (ms + eps) up to fp32 rounding of each h_k
+    rng = np.random.default_rng(int(sigma * 100))
+    x = (rng.standard_normal((3, 4096)) * sigma).astype(np.float32)
+    h, ms = oracle_mod.rmsnorm(x)
+    eps = oracle_mod.RMS_EPS
+    got = (h.astype(np.float64) ** 2).mean(axis=1)
+    expect = ms.astype(np.float64) / (ms.astype(np.float64) + eps)
+    assert np.allclose(got, expect, rtol=1e-6, atol=0)
+
+
+def test_rmsnorm_scale_invariant_bitwise(oracle_mod):
+    # x -> 2^j x scales the mean square by 4^j exactly; with eps below half an
+    # ulp of both mean squares, r scales by 2^-j and h is unchanged bit for bit
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((4, 2560)) * 16).astype(np.float32)
+    h, ms = oracle_mod.rmsnorm(x)
+    assert ms.min() > 64
+    for j in (-2, 3):
+        hj, msj = oracle_mod.rmsnorm(x * np.float32(2.0 ** j))
+        assert np.array_equal(msj, ms * np.float32(4.0 ** j))
+        assert np.array_equal(hj, h)
+
+
+def test_rmsnorm_permutation_equivariant(oracle_mod):
+    # values on a grid of 2^-4 (squares exact, the fp64 sum exact in any
+    # order): permuting the columns of x and g permutes the columns of h
+    rng = np.random.default_rng(6)
+    K = 1024
+    x = (rng.integers(-200, 201, size=(3, K)) / 16.0).astype(np.float32)
+    g = (rng.integers(1, 64, size=K) / 32.0).astype(np.float32)
+    perm = rng.permutation(K)
+    h, _ = oracle_mod.rmsnorm(x, g)
+    hp, _ = oracle_mod.rmsnorm(x[:, perm], g[perm])
+    assert np.array_equal(hp, h[:, perm])
+
+
+def test_rmsnorm_mean_square_in_fp64(oracle_mod):
+    # [2^12, 1, 1, ...]: S = 2^24 + (K - 1) exactly (an fp32 running sum stays
+    # at 2^24); ms is S / K rounded to fp32
+    K = 1000
+    x = np.ones(K, np.float32)
+    x[0] = 4096.0
+    S = oracle_mod.sum_squares(x)
+    assert S == 2.0 ** 24 + K - 1
+    _, ms = oracle_mod.rmsnorm(x[None, :])
+    exact = Fraction(2 ** 24 + K - 1, K)
+    cand = np.float32(float(exact))
+    lo, hi = np.nextafter(cand, np.float32(-np.inf)), np.nextafter(cand, np.float32(np.inf))
+    best = min((cand, lo, hi), key=lambda v: abs(Fraction(float(v)) - exact))
+    assert ms[0] == best
+
+
+def test_rmsnorm_matches_torch_module(oracle_mod):
+    # torch.nn.RMSNorm (the norm of the BitTransformer block) in fp64 with the
+    # same eps and weight: the oracle's fp32 h is within its six roundings
+    import torch
+
+    rng = np.random.default_rng(8)
+    M, K = 5, 2560
+    x = (rng.standard_normal((M, K)) * np.exp(rng.standard_normal((M, 1)))).astype(np.float32)
+    g = (1.0 + 0.1 * rng.standard_normal(K)).astype(np.float32)
+    norm = torch.nn.RMSNorm(K, eps=oracle_mod.RMS_EPS, dtype=torch.float64)
+    with torch.no_grad():
+        norm.weight.copy_(torch.from_numpy(g.astype(np.float64)))
+        ref = norm(torch.from_numpy(x.astype(np.float64))).numpy()
+    h, _ = oracle_mod.rmsnorm(x, g)
+    assert np.all(np.abs(h - ref) <= 8 * 2.0 ** -24 * np.abs(ref))
+
+
+def test_bitlinear_rmsnorm_is_scale_invariant(oracle_mod):
+    # the normed BitLinear ignores the scale of its input (powers of two,
+    # bit for bit), where the plain BitLinear scales with it
+    rng = np.random.default_rng(9)
+    N, K = 64, 512
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    packed, beta, _ = oracle_mod.pack_weights(W)
+    x = (rng.standard_normal((3, K)) * 20).astype(np.float32)
+    x[2] = 0.0  # a zero token: h = 0, scale 1e-8, y = 0
+    g = (1.0 + 0.1 * rng.standard_normal(K)).astype(np.float32)
+    y, acc, xq, s, h, ms = oracle_mod.bitlinear_rmsnorm(x, g, packed, beta, N, K)
+    y2, acc2, xq2, s2, _, _ = oracle_mod.bitlinear_rmsnorm(x * np.float32(8.0), g, packed, beta, N, K)
+    assert np.array_equal(xq, xq2) and np.array_equal(acc, acc2) and np.array_equal(y, y2)
+    assert np.all(xq[2] == 0) and np.all(y[2] == 0.0) and s[2] == np.float32(1e-8)
+    # and it is the plain BitLinear of the normed activations
+    yb, accb, xqb, sb = oracle_mod.bitlinear(h, packed, beta, N, K)
+    assert np.array_equal(y, yb) and np.array_equal(xq, xqb)
