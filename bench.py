@@ -65,6 +65,9 @@ def parse():
     ap.add_argument("--unfused", action="store_true",
                     help="decode step as quant_act + w2a8_gemv (two calls) instead of the fused bitlinear call")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=None,
+                    help="reference arm: seconds of oracle work per step (default: 150 s over warm-up and "
+                         "steps, 1 to 20 s each)")
     ap.add_argument("--group", type=int, default=0,
                     help="group-wise weight scales: G consecutive weights of a row per scale (0: one beta per matrix)")
     return ap.parse_args()
@@ -759,7 +762,7 @@ def run_reference(args):
     sample, M = oracle_sample(args)
     unit, div = metric_unit(args.workload)
     cores = os.cpu_count() or 1
-    per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    per_step = args.ref_step_seconds or max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         time_oracle(sample, per_step / 4, cores, div)
     vals = []

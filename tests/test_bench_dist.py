@@ -61,3 +61,27 @@ def test_reference_arm_prints_on_rank_zero_only():
                         "--warmup", "0"], cwd=ROOT, env=env, capture_output=True, timeout=300)
     assert r.returncode == 0, r.stderr.decode()[-2000:]
     assert r.stdout.strip() == b""
+
+
+def test_reference_arm_json_line():
+    """The reference arm (the oracle on the host's cores) prints one JSON line
+    with the contract's keys, its own value as cpu_baseline and e2e."""
+    import json
+
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "bitlinear-1024", "--steps", "2", "--warmup", "1", "--ref-step-seconds", "0.3"],
+                       cwd=ROOT, env=env, capture_output=True, timeout=300)
+    assert r.returncode == 0, r.stderr.decode()[-2000:]
+    lines = r.stdout.decode().strip().splitlines()
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["value"] > 0
+    assert line["config"]["workload"] == "bitlinear-1024"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
