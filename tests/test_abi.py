@@ -229,3 +229,34 @@ def test_package_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(ImportError):
         _lib.load()
+
+
+def test_binding_rejects_host_tensors():
+    """The Python binding never computes on the host: every entry point
+    raises on CPU tensors before anything reaches the library."""
+    import torch
+
+    import ternary_weight_05_b300 as tw
+
+    W = torch.zeros((8, 64))
+    x = torch.zeros((1, 64), dtype=torch.bfloat16)
+    xq = torch.zeros((1, 64), dtype=torch.int8)
+    s = torch.ones(1)
+    packed = torch.zeros((8, 16), dtype=torch.uint8)
+    beta = torch.ones(1)
+    calls = [
+        lambda: tw.pack_weights(W),
+        lambda: tw.quant_act(x),
+        lambda: tw.w2a8_gemv(xq, s, packed, beta, 8, 64),
+        lambda: tw.w2a8_gemm(xq, s, packed, beta, 8, 64),
+        lambda: tw.w2a8_gemv_static_scratch(xq, s, packed, beta, 8, 64),
+        lambda: tw.bitlinear(x, packed, beta, 8, 64),
+        lambda: tw.bitlinear_swiglu(x, packed, beta, packed, beta, 8, 64),
+        lambda: tw.pack_weights_grouped(W, 32),
+        lambda: tw.w2a8_grouped(xq, s, packed, torch.ones((8, 2)), 8, 64, 32),
+        lambda: tw.bitlinear_grouped(x, packed, torch.ones((8, 2)), 8, 64, 32),
+        lambda: tw.bitlinear_fake_quant(W, x),
+    ]
+    for i, call in enumerate(calls):
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            call()
