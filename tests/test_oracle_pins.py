@@ -186,6 +186,28 @@ def test_quant_act_all_bf16_within_half_step(oracle_mod, smax):
     assert np.all(np.diff(xq[order, 1].astype(np.int32)) >= 0)
 
 
+def test_quant_act_divides_first_like_the_page_listing(oracle_mod):
+    # fp32 rows whose absmax is the first element and whose other elements
+    # round to different codes under fl(fl(x / s) * 127) and fl(x * fl(127 /
+    # s)): the absmax_quantize listing of BitNet 深度拆解 section 2.2
+    # (torch.round(x / scales * qmax), run in torch CPU fp32) decides
+    import torch
+
+    rows = [[3.3, 3.235039472579956, 1.8578739166259766],
+            [0.7071, 0.6319357752799988, -0.4314979910850525, 0.6876129508018494, 0.2978728115558624],
+            [5.123, 3.933011770248413]]
+    for r in rows:
+        x = np.array([r], np.float32)
+        xq, s = oracle_mod.quant_act(x)
+        xt = torch.from_numpy(x)
+        scales = xt.abs().amax(dim=-1, keepdim=True).clamp_min(1e-8)
+        ref = torch.clamp(torch.round(xt / scales * 127), -127, 127)
+        assert np.array_equal(xq, ref.numpy().astype(np.int8))
+        # the rows do tell the two orders apart
+        other = np.rint(x * np.float32(np.float32(127.0) / s[0])).astype(np.int8)
+        assert not np.array_equal(other, xq)
+
+
 def test_quant_act_invariants(oracle_mod):
     rng = np.random.default_rng(5)
     x = (rng.standard_t(4, size=(64, 777)) * rng.choice([1e-6, 1.0, 1e4])).astype(np.float32)
