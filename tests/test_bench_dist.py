@@ -85,3 +85,20 @@ def test_reference_arm_json_line():
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_stacks_stream_from_hbm_or_say_so():
+    """Single-matrix workloads default to enough copies to stream three times
+    the L2 per step; the line's L2 note follows the stack's actual size."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from ternary_weight_05_b300 import synth
+
+    for w in ("gateup-sweep", "bitlinear-1024"):
+        args = bench.parse(["--workload", w])
+        L = synth.workload(w).layers[0]
+        assert args.layers * L.N * L.K // 4 >= 3 * bench.L2_BYTES
+    assert bench.parse(["--workload", "2b-decode"]).layers == 30
+    assert bench.parse(["--workload", "bitlinear-1024", "--layers", "5"]).layers == 5
+    assert bench.l2_note(496e6).startswith("inputs larger than L2")
+    assert bench.l2_note(7.9e6).startswith("L2-resident")
