@@ -359,6 +359,15 @@ int bitnet_w2a8_gemv_static_scratch(const int8_t *x_q, const float *scale, int64
 int bitnet_selftest_wait_timeout(int64_t limit_ns, cudaStream_t stream);
 
 /*
+ * bitnet_test_inject_cuda_failures -- test hook for the host-side failure
+ * path: the next n entry-point calls that get past argument validation fail
+ * with BITNET_ERR_CUDA at their device query, before any other CUDA call
+ * (nothing is enqueued), as a failing cudaGetDevice would make them.  n <= 0
+ * clears the count.  Returns the count that was pending.
+ */
+int bitnet_test_inject_cuda_failures(int n);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word of the
  * current device.  Returns BITNET_OK, BITNET_ERR_TIMEOUT (a kernel's bounded
  * wait expired since the last check) or BITNET_ERR_CUDA.

@@ -34,6 +34,7 @@ SIGNATURES = {
     "bitnet_bitlinear_grouped_workspace_bytes": (_sz, [_i64, _i64]),
     "bitnet_bitlinear_fake_quant_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "bitnet_selftest_wait_timeout": (_i, [_i64, _p]),
+    "bitnet_test_inject_cuda_failures": (_i, [_i]),
     "bitnet_bitlinear_fake_quant": (_i, [_p, _i, _p, _i, _i64, _i64, _i64, _f, _f, _p, _p, _p, _p, _p, _p, _p, _p,
                                          _sz, _p]),
     "bitnet_bitlinear_grouped": (_i, [_p, _i, _i64, _p, _p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _sz, _p]),

@@ -3,6 +3,7 @@
 // included .cuh files (one translation unit, so they share the device error
 // word).
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -43,7 +44,15 @@ std::mutex g_mu;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+// Test hook (bitnet_test_inject_cuda_failures): pending injected failures of
+// the device query, consumed one per query.
+std::atomic<int> g_inject_cuda_failures{0};
+
+// Every entry point that enqueues work calls this after validating its
+// arguments and before any other CUDA call.
 bitnet_status device_info(DeviceInfo **out) {
+  for (int n = g_inject_cuda_failures.load(); n > 0; n = g_inject_cuda_failures.load())
+    if (g_inject_cuda_failures.compare_exchange_weak(n, n - 1)) return BITNET_ERR_CUDA;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BITNET_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -458,6 +467,8 @@ const char *bitnet_status_string(int status) {
 
 int bitnet_version(void) { return 100; }
 
+int bitnet_test_inject_cuda_failures(int n) { return g_inject_cuda_failures.exchange(n > 0 ? n : 0); }
+
 void bitnet_set_pdl(int enable) { t_pdl = enable ? 1 : 0; }
 
 size_t bitnet_pack_workspace_bytes(int64_t N, int64_t K) {
@@ -866,6 +877,8 @@ int bitnet_pack_weights_grouped(const void *W, int dtype, int64_t N, int64_t K, 
   if (!group_shape_ok(N, K, G)) return BITNET_ERR_SHAPE;
   if (!aligned(W, dtype == BITNET_F32 ? 4 : 2) || !aligned(w_scale, 4) || !aligned(absmean, 4))
     return BITNET_ERR_ALIGNMENT;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
   const int64_t groups = N * (K / G);
   const dim3 grid((unsigned)cdiv(groups, kPackThreads));
   return dtype == BITNET_F32

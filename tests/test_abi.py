@@ -260,3 +260,52 @@ def test_binding_rejects_host_tensors():
     for i, call in enumerate(calls):
         with pytest.raises(ValueError, match="CUDA tensor"):
             call()
+
+
+def test_injected_cuda_failure_reaches_every_caller(clib):
+    """Host-side failure path: with failures injected at the device query,
+    every entry point that enqueues work returns BITNET_ERR_CUDA after its
+    argument checks, before any other CUDA call, one injected failure each
+    (the composite calls stop at their first device query)."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("the calls below pass placeholder pointers: host-only test")
+    CUDA = 5
+    nb_bl = clib.bitnet_bitlinear_workspace_bytes(2, 8, 64)
+    nb_sw = clib.bitnet_bitlinear_swiglu_workspace_bytes(2, 8, 64)
+    nb_gr = clib.bitnet_bitlinear_grouped_workspace_bytes(2, 256)
+    nb_fq = clib.bitnet_bitlinear_fake_quant_workspace_bytes(2, 8, 64)
+    nb_pk = clib.bitnet_pack_workspace_bytes(16, 64)
+    calls = {
+        "pack_weights": lambda: clib.bitnet_pack_weights(FAKE, 0, 16, 64, 1.0, 1e-8, FAKE, FAKE, None, FAKE, nb_pk,
+                                                         None),
+        "quant_act": lambda: clib.bitnet_quant_act(FAKE, 0, 1, 8, FAKE, FAKE, None),
+        "w2a8_gemv": lambda: clib.bitnet_w2a8_gemv(FAKE, FAKE, 1, FAKE, FAKE, 8, 64, FAKE, None, FAKE, 1 << 20, None),
+        "w2a8_gemm": lambda: clib.bitnet_w2a8_gemm(FAKE, FAKE, 300, FAKE, FAKE, 8, 64, FAKE, None, FAKE, 1 << 22,
+                                                   None),
+        "static_scratch": lambda: clib.bitnet_w2a8_gemv_static_scratch(FAKE, FAKE, 1, FAKE, FAKE, 8, 64, FAKE, None,
+                                                                      None),
+        "bitlinear": lambda: clib.bitnet_bitlinear(FAKE, 1, 1, FAKE, FAKE, 8, 64, FAKE, None, None, None, FAKE, nb_bl,
+                                                   None),
+        "swiglu": lambda: clib.bitnet_bitlinear_swiglu(FAKE, 0, 2, FAKE, FAKE, FAKE, FAKE, 8, 64, FAKE, None, None,
+                                                       None, None, FAKE, nb_sw, None),
+        "pack_grouped": lambda: clib.bitnet_pack_weights_grouped(FAKE, 0, 4, 256, 128, 1.0, 1e-8, FAKE, FAKE, None,
+                                                                 None),
+        "w2a8_grouped": lambda: clib.bitnet_w2a8_grouped(FAKE, FAKE, 1, FAKE, FAKE, 8, 256, 64, FAKE, None, None),
+        "bitlinear_grouped": lambda: clib.bitnet_bitlinear_grouped(FAKE, 1, 2, FAKE, FAKE, 8, 256, 64, FAKE, None,
+                                                                   None, None, FAKE, nb_gr, None),
+        "fake_quant": lambda: clib.bitnet_bitlinear_fake_quant(FAKE, 0, FAKE, 1, 2, 8, 64, 1.0, 1e-8, None, FAKE,
+                                                               None, None, None, None, None, FAKE, nb_fq, None),
+        "selftest": lambda: clib.bitnet_selftest_wait_timeout(2_000_000, None),
+    }
+    n = len(calls) + 3
+    assert clib.bitnet_test_inject_cuda_failures(n) == 0
+    try:
+        for i, (name, call) in enumerate(calls.items()):
+            assert call() == CUDA, name
+            # exactly one injected failure consumed: the call went no further
+            left = clib.bitnet_test_inject_cuda_failures(n - i - 1)
+            assert left == n - i - 1, (name, left)
+    finally:
+        assert clib.bitnet_test_inject_cuda_failures(0) == 3
