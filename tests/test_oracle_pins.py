@@ -90,6 +90,29 @@ def test_ternarize_thresholds_at_half_gamma(oracle_mod):
         assert oracle_mod.ternarize(1.0, w) == want, w
 
 
+@pytest.mark.parametrize("R", [4.0, 0.05, 300.0])
+def test_pack_every_bf16_weight_like_the_page_listing(oracle_mod, R):
+    # Every finite bf16 weight with |w| <= R in one matrix (so mean|W|, and
+    # with it gamma, differ per R): the oracle's codes equal the absmean
+    # listing of BitNet 深度拆解 section 2.2 run in torch CPU fp32 on the same
+    # mean (gamma = 1 / (alpha * mean + eps), clamp(round(gamma * w), -1, 1)),
+    # and beta is the listing's mean(|W_ternary|).
+    import torch
+
+    v = _all_finite_bf16()
+    v = v[np.abs(v) <= R]
+    n = v.size - v.size % 4
+    W = v[:n].reshape(4, n // 4).astype(np.float32)
+    packed, beta, am = oracle_mod.pack_weights(W)
+    Wt = torch.from_numpy(W)
+    gamma = 1.0 / (1.0 * torch.tensor(am, dtype=torch.float32) + 1e-8)
+    wt = torch.clamp(torch.round(gamma * Wt), -1, 1)
+    assert np.array_equal(oracle_mod.unpack_codes(packed, W.size), wt.numpy().astype(np.int8).ravel())
+    assert beta == np.float32(float(wt.abs().mean(dtype=torch.float64)))  # nnz / n, rounded once
+    # and codes of both signs and zeros occur
+    assert {-1, 0, 1} <= set(np.unique(wt.numpy()).astype(int).tolist())
+
+
 def test_absmean_equals_exact_mean_to_fp32_rounding(oracle_mod):
     rng = np.random.default_rng(3)
     for n in [1, 5, 4095, 4096, 4097, 20000]:
