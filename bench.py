@@ -776,10 +776,14 @@ def cpu_baseline(args):
         sample, M = oracle_sample(args)
         cores = os.cpu_count() or 1
         v, el, passes = time_oracle(sample, args.cpu_seconds, cores, div)
+        # the same sample on one thread, for the scaling of the oracle itself
+        v1, el1, passes1 = time_oracle(sample, min(6.0, args.cpu_seconds / 2), 1, div)
         names = ",".join(name for name, *_ in sample)
         return {"value": round(v, 4), "unit": unit, "cores": cores, "kind": "oracle",
                 "sample": f"{passes} pass(es) over one layer ({names}; M={M}) in {el:.1f} s, "
-                          f"rows split over {cores} threads"}
+                          f"rows split over {cores} threads",
+                "value_1thread": round(v1, 4),
+                "sample_1thread": f"{passes1} pass(es) over the same layer in {el1:.1f} s on one thread"}
     except Exception as ex:  # the baseline must never break the GPU line
         return {"value": None, "unit": unit, "cores": os.cpu_count(), "kind": "oracle", "sample": f"failed: {ex}"}
 

@@ -102,3 +102,15 @@ def test_stacks_stream_from_hbm_or_say_so():
     assert bench.parse(["--workload", "bitlinear-1024", "--layers", "5"]).layers == 5
     assert bench.l2_note(496e6).startswith("inputs larger than L2")
     assert bench.l2_note(7.9e6).startswith("L2-resident")
+
+
+def test_cpu_baseline_object():
+    """The native line's cpu_baseline: the oracle on all host cores and on one
+    thread, over a bounded sample of the workload."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    cb = bench.cpu_baseline(bench.parse(["--workload", "bitlinear-1024", "--cpu-seconds", "0.4"]))
+    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s" and cb["cores"] >= 1
+    assert cb["value"] > 0 and cb["value_1thread"] > 0
+    assert "pass(es)" in cb["sample"] and "one thread" in cb["sample_1thread"]
