@@ -82,7 +82,7 @@ size_t bitnet_pack_workspace_bytes(int64_t N, int64_t K);
  * gamma = 1/(fl32(alpha*mean) + eps) in fp32; code = clamp(rint(fl32(gamma*w)),
  * -1, 1) + 1 with round-half-even (a NaN product gives code 1).
  * Errors: INVALID_ARG (null W/packed/beta, bad dtype, non-finite alpha or eps),
- * SHAPE (N, K <= 0, K % 4 != 0), WORKSPACE, CUDA.
+ * SHAPE (N, K <= 0, K % 4 != 0), ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA.
  */
 int bitnet_pack_weights(const void *W, int dtype, int64_t N, int64_t K, float alpha, float eps,
                         uint8_t *packed, float *beta, float *absmean, void *workspace,
@@ -96,12 +96,12 @@ int bitnet_pack_weights(const void *W, int dtype, int64_t N, int64_t K, float al
  *   x_q    device, [M, K] int8 out: clamp(rint(fl32(fl32(x/s) * 127)), -127, 127).
  *   scale  device, [M] float out: s = max(max_k |x[m,k]|, fl32(1e-8)) (the
  *          absmax itself, not absmax/127).
- * Errors: INVALID_ARG, SHAPE (M, K <= 0), CUDA.
+ * Errors: INVALID_ARG, SHAPE (M, K <= 0), ALIGNMENT, UNSUPPORTED, CUDA.
  */
 int bitnet_quant_act(const void *x, int dtype, int64_t M, int64_t K, int8_t *x_q, float *scale,
                      cudaStream_t stream);
 
-/* Workspace bytes bitnet_w2a8_gemv needs (0 is never returned). */
+/* Workspace bytes bitnet_w2a8_gemv needs (0 for shapes the call rejects). */
 size_t bitnet_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
@@ -123,7 +123,7 @@ size_t bitnet_gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * Packed codes equal to 3 never come out of bitnet_pack_weights; the GEMV
  * does not define a result for them.
  * Errors: INVALID_ARG, SHAPE (M outside 1..64, N, K <= 0, K % 4 != 0),
- * WORKSPACE, CUDA.
+ * ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA.
  */
 int bitnet_w2a8_gemv(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
                      const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc,
@@ -144,6 +144,7 @@ size_t bitnet_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *             uses, in stream order; no state is kept between calls).
  * Shapes outside the tensor-core path (K % 64 != 0, K < 512, K > 65536,
  * unaligned pointers) run a plain CUDA-core kernel with the same results.
+ * Errors: as bitnet_w2a8_gemv (any M >= 1).
  */
 int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
                      const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc,
@@ -231,7 +232,7 @@ int bitnet_bitlinear_swiglu(const void *x, int dtype, int64_t M, const uint8_t *
  *   packed   device, N * K / 4 bytes out, the same layout as bitnet_pack_weights.
  *   w_scale  device, [N, K / G] float out: beta per group.
  *   absmean  device, [N, K / G] float out (mean|W_g|), or NULL.
- * No workspace.  Errors: INVALID_ARG, SHAPE, ALIGNMENT, CUDA.
+ * No workspace.  Errors: INVALID_ARG, SHAPE, ALIGNMENT, UNSUPPORTED, CUDA.
  */
 int bitnet_pack_weights_grouped(const void *W, int dtype, int64_t N, int64_t K, int64_t G, float alpha,
                                 float eps, uint8_t *packed, float *w_scale, float *absmean,
@@ -242,8 +243,8 @@ int bitnet_pack_weights_grouped(const void *W, int dtype, int64_t N, int64_t K, 
  *   y[m, n] = fl(F * fl(s_m / 127)),  F = sum_g acc_g[m, n] * w_scale[n, g]
  * where acc_g is the exact int32 product of group g (sum over its K range of
  * (code - 1) * x_q) and F is formed in fp32 (one rounding per group term and
- * per addition; the order is the kernel's).  The relative error of y against
- * the exact value is at most about (K / G + 3) * 2^-24 of
+ * per addition; the order is the kernel's).  The error of y against the
+ * exact value is at most (K / G + 8) * 2^-24 times
  * (s_m / 127) * sum_g |acc_g * w_scale[n, g]|.
  * One or two tokens (K % 64 == 0, K <= 8192 / 4096, G = K or a power of two
  * from 64 to 2048, x_q and packed 16-byte aligned) stream through one kernel
@@ -252,7 +253,7 @@ int bitnet_pack_weights_grouped(const void *W, int dtype, int64_t N, int64_t K, 
  *   w_scale  device, [N, K / G] float (any values, e.g. beta or mean|W_g|).
  *   y        device, [M, N] float out.
  *   acc_g    device, [M, N, K / G] int32 out (per-group products), or NULL.
- * Errors: INVALID_ARG, SHAPE, ALIGNMENT, CUDA.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, UNSUPPORTED, CUDA.
  */
 int bitnet_w2a8_grouped(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
                         const float *w_scale, int64_t N, int64_t K, int64_t G, float *y,
@@ -272,7 +273,7 @@ size_t bitnet_bitlinear_grouped_workspace_bytes(int64_t M, int64_t K);
  *   workspace device, >= bitnet_bitlinear_grouped_workspace_bytes(M, K),
  *            256-byte aligned, any contents.
  *   other arguments as bitnet_w2a8_grouped.
- * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE, CUDA.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA.
  */
 int bitnet_bitlinear_grouped(const void *x, int dtype, int64_t M, const uint8_t *packed,
                              const float *w_scale, int64_t N, int64_t K, int64_t G, float *y,
@@ -302,7 +303,7 @@ size_t bitnet_bitlinear_fake_quant_workspace_bytes(int64_t M, int64_t N, int64_t
  *   x_q, scale, acc: device outs as bitnet_bitlinear, or NULL.
  *   workspace device, >= bitnet_bitlinear_fake_quant_workspace_bytes(M, N, K),
  *            256-byte aligned, any contents.
- * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE, CUDA.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA.
  */
 int bitnet_bitlinear_fake_quant(const void *W, int w_dtype, const void *x, int x_dtype, int64_t M,
                                 int64_t N, int64_t K, float alpha, float eps,
