@@ -1,18 +1,24 @@
 #!/usr/bin/env python3
-"""Throughput of the BitNet b1.58 W2A8 path on B300: packed-weight GB/s.
+"""Throughput of the BitNet b1.58 W2A8 path on B300.
 
-One step = one decode pass of one token through a stack of BitLinear layers
-shaped like a ~2B BitNet model (per layer: q/o 2560x2560, gate/up 6912x2560,
-down 2560x6912; 30 layers, 496 MB of packed 2-bit weights, about 4x the L2),
-each GEMV preceded by the per-token int8 quantisation of its own activation.
-Weights are packed once before timing (offline step).  The stack is larger
-than L2, so every step reads its weights from HBM.
+Default line (N=1): the 100B-class layer stream, the largest configuration
+that fits one GPU: 30 distinct BitLinear layers of 28672 x 8192 ternary
+weights (58.7 MB of packed 2-bit codes each, 1.76 GB per pass, 14x the L2),
+bf16 activations quantised per token inside the streaming kernel.  One pass
+= one token through the 30 layers; one step = a decode of `--tokens` tokens
+(192 by default, so that 20 timed steps last about a second).  `value` is
+packed-weight GB/s.  The same line carries a `prefill` object: the prefill
+GEMM workload (M = 2048 tokens against 6912 x 2560 and 2560 x 6912), in
+TOPS, timed in the same run.  Weights are packed once before timing (the
+offline step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl reference]
 
-Prints one JSON line (rank 0).  Under torchrun every rank runs its own copy
-of the stack (independent token streams, no collective on the data path).
+Prints one JSON line (rank 0).  Under torchrun the ranks split every matrix
+by output rows (each rank streams its N / world rows of every layer, x is
+replicated, each rank keeps its slice of y: no collective on the data path);
+`--replicas` runs independent copies of the whole stack instead.
 """
 from __future__ import annotations
 
@@ -78,7 +84,7 @@ def parse(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="2b-decode",
+    ap.add_argument("--workload", default="100b-stream",
                     choices=["2b-decode", "100b-stream", "gateup-sweep", "prefill-2048", "bitlinear-1024",
                              "ffn-2b-decode"])
     ap.add_argument("--layers", type=int, default=None,
@@ -95,9 +101,18 @@ def parse(argv=None):
                          "steps, 1 to 20 s each)")
     ap.add_argument("--group", type=int, default=0,
                     help="group-wise weight scales: G consecutive weights of a row per scale (0: one beta per matrix)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="decode workloads: tokens per step, each one pass over the stack (default: 192 for "
+                         "100b-stream, so that 20 steps last about a second; 1 otherwise)")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="100b-stream: leave out the prefill GEMM object of the line")
+    ap.add_argument("--replicas", action="store_true",
+                    help="N > 1: every rank runs the whole stack (independent replicas) instead of its rows")
     args = ap.parse_args(argv)
     if args.layers is None:
         args.layers = default_layers(args.workload)
+    if args.tokens is None:
+        args.tokens = 192 if args.workload == "100b-stream" else 1
     return args
 
 
@@ -194,14 +209,17 @@ def decode_layers(args):
     return wl, layers, M
 
 
-def build_stack(args, dev, rank):
-    """Packs every weight matrix on the device (offline step, not timed)."""
+def build_stack(args, dev, rank, world=1):
+    """Packs every weight matrix on the device (offline step, not timed).
+    With world > 1 (row split) each rank keeps the packed rows of its range
+    of every matrix and computes that slice of y."""
     import torch
 
     import ternary_weight_05_b300 as tw
-    from ternary_weight_05_b300 import synth
+    from ternary_weight_05_b300 import shard, synth
 
     wl, layers, M = decode_layers(args)
+    split = world > 1 and not args.replicas
     stack = []
     for L, rep in layers:
         W = synth.weights_torch(L.N, L.K, L.w_dist, L.w_scale, L.w_seed + 1000 * rep, dev)
@@ -210,15 +228,68 @@ def build_stack(args, dev, rank):
         else:
             packed, beta, _ = tw.pack_weights(W)
         del W
-        x = synth.acts_torch(M, L.K, L.x_dist, L.x_seed + 1000 * rep + 7919 * rank, dev, outlier_p=L.outlier_p)
+        r0, r1 = shard.row_bounds(L.N, world, rank) if split else (0, L.N)
+        if split:
+            packed = shard.packed_rows(packed, L.K, r0, r1).clone()
+            if args.group:
+                beta = beta[r0:r1].clone()
+        # the activations: the same on every rank when the rows are split,
+        # an independent token stream per replica otherwise
+        xs = L.x_seed + 1000 * rep + (0 if split else 7919 * rank)
+        x = synth.acts_torch(M, L.K, L.x_dist, xs, dev, outlier_p=L.outlier_p)
         if not L.x_bf16:
             x = x.float()
-        stack.append(dict(L=L, packed=packed, beta=beta, x=x, M=M,
+        n = r1 - r0
+        stack.append(dict(L=L, n=n, r0=r0, packed=packed, beta=beta, x=x, M=M,
                           xq=torch.empty((M, L.K), dtype=torch.int8, device=dev),
                           s=torch.empty(M, dtype=torch.float32, device=dev),
-                          y=torch.empty((M, L.N), dtype=torch.float32, device=dev)))
+                          y=torch.empty((M, n), dtype=torch.float32, device=dev)))
     torch.cuda.synchronize(dev)
     return wl, stack, M
+
+
+def decode_layer_fn(ws, fused, G):
+    """One BitLinear of a decode stack entry as the benchmark runs it: the
+    fused call (quantisation inside the streaming kernel), or quant_act and
+    the matmul (`quant` False: the matmul alone)."""
+    import ternary_weight_05_b300 as tw
+
+    def layer(e, quant):
+        L, n = e["L"], e["n"]
+        if fused and G:
+            tw.bitlinear_grouped(e["x"], e["packed"], e["beta"], n, L.K, G, out=e["y"], workspace=ws)
+        elif fused:
+            tw.bitlinear(e["x"], e["packed"], e["beta"], n, L.K, out=e["y"], workspace=ws)
+        else:
+            if quant:
+                tw.quant_act(e["x"], out=(e["xq"], e["s"]))
+            if G:
+                tw.w2a8_grouped(e["xq"], e["s"], e["packed"], e["beta"], n, L.K, G, out=e["y"])
+            else:
+                tw.w2a8_gemv(e["xq"], e["s"], e["packed"], e["beta"], n, L.K, out=e["y"], workspace=ws)
+
+    return layer
+
+
+def passes_per_graph(tokens):
+    """Passes over the stack captured in one graph: a step's passes are then
+    tokens / ppg replays of it."""
+    return max(d for d in (16, 8, 4, 2, 1) if tokens % d == 0)
+
+
+def capture_passes(stack, ws, fused, G, ppg, stream):
+    """The benchmark's CUDA graph: ppg passes over the stack's BitLinears
+    (launched with the calling thread's PDL setting), captured on `stream`."""
+    import torch
+
+    layer = decode_layer_fn(ws, fused, G)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(ppg):
+            for e in stack:
+                if e["n"] > 0:
+                    layer(e, True)
+    return graph
 
 
 def max_over_ranks(values, device):
@@ -262,54 +333,52 @@ def run_native(args):
     if args.workload == "ffn-2b-decode":
         return run_ffn(args, dev, rank, world, hbm_peak, peak_src)
 
-    wl, stack, M = build_stack(args, dev, rank)
+    wl, stack, M = build_stack(args, dev, rank, world)
+    split = world > 1 and not args.replicas
     fused = not args.unfused
     G = args.group
-    max_ws = max(max(tw.gemv_workspace_bytes(M, e["L"].N, e["L"].K), tw.bitlinear_workspace_bytes(M, e["L"].N,
-                                                                                                 e["L"].K))
-                 for e in stack)
+    T = args.tokens
+    max_ws = max(max(tw.gemv_workspace_bytes(M, max(e["n"], 1), e["L"].K),
+                     tw.bitlinear_workspace_bytes(M, max(e["n"], 1), e["L"].K)) for e in stack)
     ws = torch.zeros(max_ws, dtype=torch.uint8, device=dev)
-    # weight bytes streamed per step: packed codes (+ fp32 group scales)
-    wbytes = sum(e["L"].N * e["L"].K // 4 + (4 * e["L"].N * (e["L"].K // G) if G else 0) for e in stack)
+    # weight bytes this rank streams per pass: packed codes (+ fp32 group scales)
+    wbytes = sum(e["n"] * e["L"].K // 4 + (4 * e["n"] * (e["L"].K // G) if G else 0) for e in stack)
+    # the whole job's per pass: every rank's rows (split) or every replica's stack
+    job_bytes = (sum(e["L"].N * e["L"].K // 4 + (4 * e["L"].N * (e["L"].K // G) if G else 0) for e in stack)
+                 * (1 if split else world))
     xes = stack[0]["x"].element_size()
     if fused:
         # fused BitLinear kernel: weights + x (bf16/fp32) + w_scale + y
-        gemv_bytes = wbytes + sum(xes * M * e["L"].K + (0 if G else 4) + 4 * M * e["L"].N for e in stack)
+        gemv_bytes = wbytes + sum(xes * M * e["L"].K + (0 if G else 4) + 4 * M * e["n"] for e in stack)
     else:
         # GEMV: weights + x_q + scales + w_scale + y
-        gemv_bytes = wbytes + sum(M * e["L"].K + 4 * M + (0 if G else 4) + 4 * M * e["L"].N for e in stack)
+        gemv_bytes = wbytes + sum(M * e["L"].K + 4 * M + (0 if G else 4) + 4 * M * e["n"] for e in stack)
+    active = [e for e in stack if e["n"] > 0]
+    layer = decode_layer_fn(ws, fused, G)
 
-    def layer(e, quant):
-        L = e["L"]
-        if fused and G:
-            tw.bitlinear_grouped(e["x"], e["packed"], e["beta"], L.N, L.K, G, out=e["y"], workspace=ws)
-        elif fused:
-            tw.bitlinear(e["x"], e["packed"], e["beta"], L.N, L.K, out=e["y"], workspace=ws)
-        else:
-            if quant:
-                tw.quant_act(e["x"], out=(e["xq"], e["s"]))
-            if G:
-                tw.w2a8_grouped(e["xq"], e["s"], e["packed"], e["beta"], L.N, L.K, G, out=e["y"])
-            else:
-                tw.w2a8_gemv(e["xq"], e["s"], e["packed"], e["beta"], L.N, L.K, out=e["y"], workspace=ws)
-
-    def step():
-        for e in stack:
+    def one_pass():
+        for e in active:
             layer(e, True)
+
+    ppg = passes_per_graph(T)
 
     tw.set_pdl(not args.no_pdl)
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
-        step()
+        one_pass()
         torch.cuda.synchronize(dev)
-        graph = None
-        if not args.no_graph:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                step()
-        run = graph.replay if graph is not None else step
+        graph = None if args.no_graph else capture_passes(stack, ws, fused, G, ppg, stream)
+
+        def step():
+            if graph is not None:
+                for _ in range(T // ppg):
+                    graph.replay()
+            else:
+                for _ in range(T):
+                    one_pass()
+
         for _ in range(args.warmup):
-            run()
+            step()
         torch.cuda.synchronize(dev)
         if world > 1:
             dist.barrier()
@@ -320,63 +389,80 @@ def run_native(args):
         torch.cuda.synchronize(dev)
         e0.record(stream)
         for _ in range(args.steps):
-            run()
+            step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         ms_total = e0.elapsed_time(e1)
+        passes = args.steps * T
 
-        # GEMV kernel duration: a graph holding only the GEMV launches of the
-        # stack (same inputs, same launch configuration, weights colder than
-        # L2 since the stack exceeds it), replayed between two events.  In
-        # the fused form the GEMV kernel is the whole step.
-        gemv_graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gemv_graph, stream=stream):
-            for e in stack:
-                layer(e, False)
-        for _ in range(2):
-            gemv_graph.replay()
-        n_meas = max(3, args.steps)
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(n_meas):
-            gemv_graph.replay()
-        g1.record(stream)
-        torch.cuda.synchronize(dev)
+        if fused:
+            # the fused step is nothing but the GEMV kernel launches: their
+            # duration is the timed region's
+            gemv_ms, n_meas = ms_total, passes
+        else:
+            # the GEMV launches alone: a graph of the stack's GEMV calls (same
+            # inputs, same launch configuration), replayed between two events
+            gemv_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gemv_graph, stream=stream):
+                for e in active:
+                    layer(e, False)
+            for _ in range(2):
+                gemv_graph.replay()
+            n_meas = max(3, args.steps)
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record(stream)
+            for _ in range(n_meas):
+                gemv_graph.replay()
+            g1.record(stream)
+            torch.cuda.synchronize(dev)
+            gemv_ms = g0.elapsed_time(g1)
+        gemv_launches = n_meas * len(active)
         clk = clocks.stop()
-        gemv_ms = g0.elapsed_time(g1)
-        gemv_launches = n_meas * len(stack)
 
-        # end to end through the public API with host buffers
-        tw.set_pdl(False)
-        hx = [e["x"].cpu().pin_memory() for e in stack]
-        hy = [torch.empty(e["y"].shape, dtype=torch.float32).pin_memory() for e in stack]
-        h2d = sum(t.numel() * t.element_size() for t in hx)
-        d2h = sum(t.numel() * t.element_size() for t in hy)
+        # end to end through the public API: per pass, the layers' activations
+        # from pinned host memory in one copy, one bitlinear call per layer
+        # (PDL on, as a user enables it), every output back to pinned host
+        # memory in one copy
+        xsz = [e["x"].numel() for e in active]
+        ysz = [e["y"].numel() for e in active]
+        hx = torch.cat([e["x"].reshape(-1) for e in active]).cpu().pin_memory()
+        hy = torch.empty(sum(ysz), dtype=torch.float32).pin_memory()
+        dx = torch.empty_like(hx, device=dev)
+        dy = torch.empty(sum(ysz), dtype=torch.float32, device=dev)
+        xv, yv, ox, oy = [], [], 0, 0
+        for e, nx, ny in zip(active, xsz, ysz):
+            xv.append(dx[ox:ox + nx].view(e["x"].shape))
+            yv.append(dy[oy:oy + ny].view(e["y"].shape))
+            ox += nx
+            oy += ny
+        h2d = hx.numel() * hx.element_size()
+        d2h = hy.numel() * hy.element_size()
 
-        def e2e_step():
-            for e, xh, yh in zip(stack, hx, hy):
-                xd = xh.to(dev, non_blocking=True)
+        def e2e_pass():
+            dx.copy_(hx, non_blocking=True)
+            for e, xd, yd in zip(active, xv, yv):
                 if G:
-                    y = tw.bitlinear_grouped(xd, e["packed"], e["beta"], e["L"].N, e["L"].K, G)
+                    tw.bitlinear_grouped(xd, e["packed"], e["beta"], e["n"], e["L"].K, G, out=yd, workspace=ws)
                 else:
-                    y = tw.bitlinear(xd, e["packed"], e["beta"], e["L"].N, e["L"].K)
-                yh.copy_(y, non_blocking=True)
+                    tw.bitlinear(xd, e["packed"], e["beta"], e["n"], e["L"].K, out=yd, workspace=ws)
+            hy.copy_(dy, non_blocking=True)
 
         for _ in range(2):
-            e2e_step()
+            e2e_pass()
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
+        for _ in range(args.steps * T):
+            e2e_pass()
         torch.cuda.synchronize(dev)
         e2e_s = time.perf_counter() - t0
     tw.check_device_error(stream)
+    tw.set_pdl(False)
 
     ms_step = ms_total / args.steps
     if world > 1:  # max over ranks
         ms_step, e2e_s = max_over_ranks([ms_step, e2e_s], dev)
-    value = world * wbytes / (ms_step * 1e-3) / 1e9
-    e2e_val = world * wbytes * args.steps / e2e_s / 1e9
+    value = job_bytes * T / (ms_step * 1e-3) / 1e9
+    e2e_val = job_bytes * T * args.steps / e2e_s / 1e9
     achieved = gemv_bytes * n_meas / (gemv_ms * 1e-3) / 1e9
     # kernels per BitLinear: fused M <= 2: 1; fused M >= 3: prep + tensor-core GEMV;
     # unfused: quant_act (+ prep for M >= 3) + GEMV
@@ -388,29 +474,44 @@ def run_native(args):
     else:
         per_layer = (1 if M <= 2 else 2) if fused else (2 if M <= 2 else 3)
         kname = ("gemv_ldg_kernel" if M <= 2 else "gemv_mma_kernel (+prep)") + (" (fused quant)" if fused else "")
+    if split:
+        parallelism = f"rows split over {world} ranks (each streams N/{world} rows of every layer; x replicated, " \
+                      "y left sharded: no collective)"
+    else:
+        parallelism = f"replicas x{world}"
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "strong" if split else "weak",
         "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded, weights and activations drawn on device)",
         "config": {"workload": f"{wl.name}: {wl.description}", "layers_in_stack": len(stack), "M": M,
-                   "step": ("fused bitlinear" if fused else "quant_act + w2a8_gemv") + " per layer"
+                   "tokens_per_step": T,
+                   "step": f"{T} pass(es) over the stack, one token each; "
+                           + ("fused bitlinear" if fused else "quant_act + w2a8_gemv") + " per layer"
                            + (f" with group-wise scales, G={G} (weight bytes include the fp32 scales)" if G else ""),
-                   "packed_weight_bytes_per_step": wbytes, "graph": not args.no_graph, "pdl": not args.no_pdl,
+                   "packed_weight_bytes_per_pass": job_bytes, "graph": not args.no_graph,
+                   "passes_per_graph": ppg if not args.no_graph else None, "pdl": not args.no_pdl,
                    "l2": l2_note(wbytes),
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": parallelism},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4),
-                     "traffic": MEASURED_TRAFFIC.get((args.workload, M, fused, G)),
-                     "algorithmic_bytes_per_launch": round(gemv_bytes / len(stack)),
-                     "kernel": kname, "peak_source": peak_src,
+                     "traffic": MEASURED_TRAFFIC.get((args.workload, M, fused, G)) if not split else None,
+                     "algorithmic_bytes_per_launch": round(gemv_bytes / len(active)),
+                     "kernel": kname, "peak_source": peak_src + " HBM copy",
                      "launches_timed": gemv_launches, "avg_launch_us": round(1e3 * gemv_ms / gemv_launches, 3)},
-        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": per_layer * len(stack) * args.steps,
-        "gemv_only_GBps": round(wbytes * n_meas / (gemv_ms * 1e-3) / 1e9, 2),
+        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d * T,
+                "d2h_bytes_per_step": d2h * T},
+        "gpu_launches": per_layer * len(active) * T * args.steps,
         "clocks": clk,
     }
+    if args.workload == "100b-stream" and not args.no_prefill:
+        # the other half of the metric, in the same run: the prefill GEMM
+        line["prefill"] = measure_prefill(args, dev, rank, world, bf16_peak, peak_src, sub=True)
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(args)
+        if "prefill" in line:
+            line["prefill"]["cpu_baseline"] = cpu_baseline(args, workload="prefill-2048",
+                                                           seconds=args.cpu_seconds / 2, one_thread=False)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -578,30 +679,45 @@ def run_ffn(args, dev, rank, world, hbm_peak, peak_src):
         dist.destroy_process_group()
 
 
-def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
-    """Prefill: per step, quant_act + tcgen05 GEMM for both M=2048 matrices.
-    L2 is flushed (256 MB write) between steps, outside the timed spans."""
+def measure_prefill(args, dev, rank, world, bf16_peak, peak_src, sub=False):
+    """Prefill: per step the fused BitLinear (quantisation into the tensor-core
+    operand layout, then the tcgen05 GEMM) for both M=2048 matrices.  L2 is
+    flushed (256 MB write) before every step, outside the timed spans.  With
+    the rows split over ranks each rank computes its rows of both matrices.
+
+    Returns the figures: value (TOPS of the whole job), ms per step, the GEMM
+    roofline (prep + GEMM kernels alone, CUDA events), e2e through the public
+    API with host buffers, clocks.  With sub=True (the prefill object of the
+    default line) it uses at least 10 steps and 3 warm-up steps of its own."""
     import torch
-    import torch.distributed as dist
 
     import ternary_weight_05_b300 as tw
-    from ternary_weight_05_b300 import synth
+    from ternary_weight_05_b300 import shard, synth
 
     wl = synth.workload("prefill-2048")
-    M = args.M or 2048
+    M = args.M if (args.M and not sub) else 2048
+    steps = max(args.steps, 10) if sub else args.steps
+    warmup = max(args.warmup, 3) if sub else args.warmup
+    split = world > 1 and not args.replicas
     mats = []
     for L in wl.layers:
         W = synth.weights_torch(L.N, L.K, L.w_dist, L.w_scale, L.w_seed, dev)
         packed, beta, _ = tw.pack_weights(W)
-        x = synth.acts_torch(M, L.K, L.x_dist, L.x_seed + 7919 * rank, dev)
-        mats.append(dict(L=L, packed=packed, beta=beta, x=x,
+        del W
+        r0, r1 = shard.row_bounds(L.N, world, rank) if split else (0, L.N)
+        if split:
+            packed = shard.packed_rows(packed, L.K, r0, r1).clone()
+        n = r1 - r0
+        x = synth.acts_torch(M, L.K, L.x_dist, L.x_seed + (0 if split else 7919 * rank), dev)
+        mats.append(dict(L=L, n=n, packed=packed, beta=beta, x=x,
                          xq=torch.empty((M, L.K), dtype=torch.int8, device=dev),
                          s=torch.empty(M, dtype=torch.float32, device=dev),
-                         y=torch.empty((M, L.N), dtype=torch.float32, device=dev),
-                         ws=torch.empty(tw.gemm_workspace_bytes(M, L.N, L.K), dtype=torch.uint8, device=dev),
-                         wsb=torch.zeros(tw.bitlinear_workspace_bytes(M, L.N, L.K), dtype=torch.uint8, device=dev)))
+                         y=torch.empty((M, n), dtype=torch.float32, device=dev),
+                         ws=torch.empty(tw.gemm_workspace_bytes(M, n, L.K), dtype=torch.uint8, device=dev),
+                         wsb=torch.zeros(tw.bitlinear_workspace_bytes(M, n, L.K), dtype=torch.uint8, device=dev)))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    flops = sum(2.0 * M * m["L"].N * m["L"].K for m in mats)
+    flops = sum(2.0 * M * m["n"] * m["L"].K for m in mats)
+    flops_job = sum(2.0 * M * m["L"].N * m["L"].K for m in mats) * (1 if split else world)
     tw.set_pdl(not args.no_pdl)
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
@@ -609,26 +725,29 @@ def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
             for m in mats:
                 if args.unfused:
                     tw.quant_act(m["x"], out=(m["xq"], m["s"]))
-                    tw.w2a8_gemm(m["xq"], m["s"], m["packed"], m["beta"], m["L"].N, m["L"].K, out=m["y"],
+                    tw.w2a8_gemm(m["xq"], m["s"], m["packed"], m["beta"], m["n"], m["L"].K, out=m["y"],
                                  workspace=m["ws"])
                 else:
-                    tw.bitlinear(m["x"], m["packed"], m["beta"], m["L"].N, m["L"].K, out=m["y"], workspace=m["wsb"])
+                    tw.bitlinear(m["x"], m["packed"], m["beta"], m["n"], m["L"].K, out=m["y"], workspace=m["wsb"])
 
         def gemm_only():
             for m in mats:
-                tw.w2a8_gemm(m["xq"], m["s"], m["packed"], m["beta"], m["L"].N, m["L"].K, out=m["y"],
+                tw.w2a8_gemm(m["xq"], m["s"], m["packed"], m["beta"], m["n"], m["L"].K, out=m["y"],
                              workspace=m["ws"])
 
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             step()
         torch.cuda.synchronize(dev)
         if world > 1:
+            import torch.distributed as dist
             dist.barrier()
-        clocks = ClockSampler(dev.index or 0)
-        clocks.start()
-        time.sleep(0.3)
+        clocks = None
+        if not sub:
+            clocks = ClockSampler(dev.index or 0)
+            clocks.start()
+            time.sleep(0.3)
         spans, gspans = [], []
-        for _ in range(args.steps):
+        for _ in range(steps):
             flush.fill_(1)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -637,7 +756,7 @@ def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
             spans.append((a, b))
         for m in mats:  # int8 activations for the GEMM-only timing
             tw.quant_act(m["x"], out=(m["xq"], m["s"]))
-        for _ in range(args.steps):
+        for _ in range(steps):
             flush.fill_(2)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -645,47 +764,69 @@ def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
             b.record(stream)
             gspans.append((a, b))
         torch.cuda.synchronize(dev)
-        clk = clocks.stop()
-        ms_step = sum(a.elapsed_time(b) for a, b in spans) / args.steps
-        ms_gemm = sum(a.elapsed_time(b) for a, b in gspans) / args.steps
+        clk = clocks.stop() if clocks is not None else None
+        ms_step = sum(a.elapsed_time(b) for a, b in spans) / steps
+        ms_gemm = sum(a.elapsed_time(b) for a, b in gspans) / steps
         # end to end: host activations in, host outputs out, public API
-        tw.set_pdl(False)
         hx = [m["x"].cpu().pin_memory() for m in mats]
         hy = [torch.empty(m["y"].shape, dtype=torch.float32).pin_memory() for m in mats]
+        dx = [torch.empty_like(m["x"]) for m in mats]
 
         def e2e_step():
-            for m, xh, yh in zip(mats, hx, hy):
-                y = tw.bitlinear(xh.to(dev, non_blocking=True), m["packed"], m["beta"], m["L"].N, m["L"].K)
-                yh.copy_(y, non_blocking=True)
+            for m, xh, xd, yh in zip(mats, hx, dx, hy):
+                xd.copy_(xh, non_blocking=True)
+                tw.bitlinear(xd, m["packed"], m["beta"], m["n"], m["L"].K, out=m["y"], workspace=m["wsb"])
+                yh.copy_(m["y"], non_blocking=True)
 
         e2e_step()
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        for _ in range(args.steps):
+        for _ in range(steps):
             e2e_step()
         torch.cuda.synchronize(dev)
-        e2e_s = (time.perf_counter() - t0) / args.steps
+        e2e_s = (time.perf_counter() - t0) / steps
     tw.check_device_error(stream)
+    tw.set_pdl(False)
     if world > 1:
         ms_step, e2e_s = max_over_ranks([ms_step, e2e_s], dev)
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = flops_job / (ms_step * 1e-3) / 1e12
     achieved = flops / (ms_gemm * 1e-3) / 1e12
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded, drawn on device)",
-        "config": {"workload": f"{wl.name}: {wl.description}", "M": M,
-                   "matrices": [f"{m['L'].N}x{m['L'].K}" for m in mats], "l2": "flushed between steps (256 MB)",
-                   "step": "quant_act + w2a8_gemm per matrix" if args.unfused else "fused bitlinear per matrix",
-                   "pdl": not args.no_pdl, "parallelism": f"replicas x{world}"},
+    res = {
+        "workload": f"{wl.name}: {wl.description}", "M": M,
+        "matrices": [f"{m['L'].N}x{m['L'].K}" for m in mats],
+        "value": round(value, 2), "unit": "TOPS", "steps": steps, "warmup": warmup,
+        "ms_per_step": round(ms_step, 4), "l2": "flushed before every step (256 MB write)",
+        "step": "quant_act + w2a8_gemm per matrix" if args.unfused else "fused bitlinear per matrix",
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16_peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / bf16_peak, 4), "traffic": None, "kernel": "gemm_tc_kernel (+prep)",
-                     "peak_source": peak_src + " bf16 dense burst (the GEMM runs kind::f16 MMAs)"},
-        "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TOPS",
+                     "frac": round(achieved / bf16_peak, 4), "traffic": None,
+                     "kernel": "gemm_tc_kernel (+prep)", "ms_per_call_pair": round(ms_gemm, 4),
+                     "peak_source": peak_src + " bf16 dense burst (the GEMM runs kind::f16 MMAs; tcgen05 "
+                                               "kind::i8 does not exist on sm_103a)"},
+        "e2e": {"value": round(flops_job / e2e_s / 1e12, 2), "unit": "TOPS",
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hx),
                 "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hy)},
-        "gpu_launches": (6 if args.unfused else 4) * args.steps,
-        "clocks": clk,
+        "gpu_launches": (6 if args.unfused else 4) * steps,
+    }
+    if clk is not None:
+        res["clocks"] = clk
+    return res
+
+
+def run_prefill(args, dev, rank, world, bf16_peak, peak_src):
+    """The prefill workload as the whole line (--workload prefill-2048)."""
+    import torch.distributed as dist
+
+    r = measure_prefill(args, dev, rank, world, bf16_peak, peak_src)
+    split = world > 1 and not args.replicas
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": "TOPS", "n_gpus": world, "steps": r["steps"],
+        "warmup": r["warmup"], "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+        "scaling": "strong" if split else "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic (seeded, drawn on device)",
+        "config": {"workload": r["workload"], "M": r["M"], "matrices": r["matrices"], "l2": r["l2"],
+                   "step": r["step"], "pdl": not args.no_pdl,
+                   "parallelism": f"rows split over {world} ranks" if split else f"replicas x{world}"},
+        "roofline": r["roofline"], "e2e": r["e2e"], "gpu_launches": r["gpu_launches"], "clocks": r["clocks"],
     }
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(args)
@@ -770,20 +911,27 @@ def time_oracle(sample, seconds, threads, div=1e9):
             return done / el / div, el, passes
 
 
-def cpu_baseline(args):
+def cpu_baseline(args, workload=None, seconds=None, one_thread=True):
+    """The oracle, as it stands, on the host's cores over a bounded sample of
+    the workload (and on one thread, for the oracle's own scaling)."""
+    if workload is not None:
+        args = argparse.Namespace(**{**vars(args), "workload": workload, "M": None})
+    seconds = args.cpu_seconds if seconds is None else seconds
     unit, div = metric_unit(args.workload)
     try:
         sample, M = oracle_sample(args)
         cores = os.cpu_count() or 1
-        v, el, passes = time_oracle(sample, args.cpu_seconds, cores, div)
-        # the same sample on one thread, for the scaling of the oracle itself
-        v1, el1, passes1 = time_oracle(sample, min(6.0, args.cpu_seconds / 2), 1, div)
+        v, el, passes = time_oracle(sample, seconds, cores, div)
         names = ",".join(name for name, *_ in sample)
-        return {"value": round(v, 4), "unit": unit, "cores": cores, "kind": "oracle",
-                "sample": f"{passes} pass(es) over one layer ({names}; M={M}) in {el:.1f} s, "
-                          f"rows split over {cores} threads",
-                "value_1thread": round(v1, 4),
-                "sample_1thread": f"{passes1} pass(es) over the same layer in {el1:.1f} s on one thread"}
+        res = {"value": round(v, 6), "unit": unit, "cores": cores, "kind": "oracle",
+               "sample": f"{passes} pass(es) over one layer ({names}; M={M}) in {el:.1f} s, "
+                         f"rows split over {cores} threads"}
+        if one_thread:
+            # the same sample on one thread, for the scaling of the oracle itself
+            v1, el1, passes1 = time_oracle(sample, min(6.0, seconds / 2), 1, div)
+            res["value_1thread"] = round(v1, 6)
+            res["sample_1thread"] = f"{passes1} pass(es) over the same layer in {el1:.1f} s on one thread"
+        return res
     except Exception as ex:  # the baseline must never break the GPU line
         return {"value": None, "unit": unit, "cores": os.cpu_count(), "kind": "oracle", "sample": f"failed: {ex}"}
 
@@ -815,6 +963,11 @@ def run_reference(args):
                                    f"rows split over {cores} threads"},
         "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    if args.workload == "100b-stream" and not args.no_prefill:
+        # the prefill half of the metric: the oracle on its bounded sample
+        pf = cpu_baseline(args, workload="prefill-2048", seconds=min(10.0, per_step), one_thread=False)
+        line["prefill"] = {"workload": "prefill-2048", "value": pf["value"], "unit": pf["unit"],
+                           "cpu_baseline": pf}
     print(json.dumps(line), flush=True)
 
 

@@ -336,12 +336,14 @@ int bitnet_bitlinear_fake_quant(const void *W, int w_dtype, const void *x, int x
  *   - Set-up: the first call on each device looks up the array's device
  *     address (cudaGetSymbolAddress, with that device current) and caches it.
  *     Make that first call outside any stream capture.
- *   - Sharing: every call, on every stream, uses the same array.  The call
- *     zeroes the part it needs (cudaMemsetAsync on `stream`) before the
- *     kernel, so stale contents from an earlier call do not matter, but two
- *     calls that can overlap on the GPU (different streams, no ordering
- *     between them) race on the array and give wrong results.  Order them on
- *     one stream, or use bitnet_w2a8_gemv with separate workspaces.
+ *   - Sharing: every call, on every stream, uses the same array, and the
+ *     array keeps the last call's contents.  Stale contents do not matter:
+ *     like bitnet_w2a8_gemv with any workspace, the call zeroes, in stream
+ *     order, the part it accumulates into (for M <= 2 the streaming kernels
+ *     do not touch the array at all).  Two calls that can overlap on the GPU
+ *     (different streams, no ordering between them) race on the array and
+ *     give wrong results.  Order them on one stream, or use
+ *     bitnet_w2a8_gemv with separate workspaces.
  * Errors: as bitnet_w2a8_gemv, plus TOO_LARGE; WORKSPACE never occurs.
  */
 int bitnet_w2a8_gemv_static_scratch(const int8_t *x_q, const float *scale, int64_t M,

@@ -33,8 +33,30 @@ def _L():
     return _lib.load()
 
 
+try:  # the raw handle of the current stream, without building a Stream object
+    _raw_stream = torch._C._cuda_getCurrentRawStream
+except AttributeError:  # pragma: no cover
+    _raw_stream = None
+
+
 def _stream(dev: torch.device) -> int:
+    if _raw_stream is not None:
+        return _raw_stream(dev.index if dev.index is not None else torch.cuda.current_device())
     return torch.cuda.current_stream(dev).cuda_stream
+
+
+# Workspace sizes answered by the library, per (query, shape): the size
+# queries are pure functions of the shape, so each is asked once.
+_ws_sizes = {}
+
+
+def _ws_bytes(query: str, *shape) -> int:
+    key = (query, shape)
+    v = _ws_sizes.get(key)
+    if v is None:
+        v = int(getattr(_L(), query)(*shape))
+        _ws_sizes[key] = v
+    return v
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -81,10 +103,15 @@ def check_device_error(stream=None) -> None:
 
 
 class _WorkspaceCache:
-    """Zero-filled device workspaces keyed by (device, kind, shape).
+    """Device workspaces for calls made without an explicit one, keyed by
+    (device, kind, stream).
 
-    The GEMV keeps its workspace zero-filled between calls, so one buffer per
-    shape is reused; calls on different streams must not share one.
+    Every entry point takes its workspace with any contents (the kernels
+    zero, in stream order, whatever they accumulate into), so one buffer per
+    key is reused across shapes; calls on different streams get different
+    buffers.  A buffer is replaced by a larger one when a larger shape
+    arrives, and the old one is freed: a CUDA-graph capture must therefore
+    pass an explicit workspace that outlives the graph.
     """
 
     def __init__(self):
@@ -147,10 +174,9 @@ def _matmul(fn_name, ws_fn, kind, x_q, scale, packed, w_scale, N, K, want_acc, o
     dev = x_q.device
     y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=dev)
     acc = torch.empty((M, N), dtype=torch.int32, device=dev) if want_acc else None
-    nbytes = int(ws_fn(M, N, K))
     stream = _stream(dev)
     if workspace is None:
-        workspace = _ws.get(dev, kind, nbytes, stream)
+        workspace = _ws.get(dev, kind, _ws_bytes(ws_fn, M, N, K), stream)
     st = getattr(_L(), fn_name)(x_q.data_ptr(), scale.data_ptr(), M, packed.data_ptr(), w_scale.data_ptr(), N, K,
                                 y.data_ptr(), acc.data_ptr() if acc is not None else None,
                                 workspace.data_ptr(), workspace.numel(), stream)
@@ -160,13 +186,13 @@ def _matmul(fn_name, ws_fn, kind, x_q, scale, packed, w_scale, N, K, want_acc, o
 
 def w2a8_gemv(x_q, scale, packed, w_scale, N: int, K: int, want_acc: bool = False, out=None, workspace=None):
     """Decode GEMV (M <= 64): y [M, N] fp32 (and the exact int32 acc if asked)."""
-    return _matmul("bitnet_w2a8_gemv", _L().bitnet_gemv_workspace_bytes, "gemv", x_q, scale, packed, w_scale, N, K,
+    return _matmul("bitnet_w2a8_gemv", "bitnet_gemv_workspace_bytes", "gemv", x_q, scale, packed, w_scale, N, K,
                    want_acc, out, workspace)
 
 
 def w2a8_gemm(x_q, scale, packed, w_scale, N: int, K: int, want_acc: bool = False, out=None, workspace=None):
     """Prefill GEMM (any M): y [M, N] fp32 (and the exact int32 acc if asked)."""
-    return _matmul("bitnet_w2a8_gemm", _L().bitnet_gemm_workspace_bytes, "gemm", x_q, scale, packed, w_scale, N, K,
+    return _matmul("bitnet_w2a8_gemm", "bitnet_gemm_workspace_bytes", "gemm", x_q, scale, packed, w_scale, N, K,
                    want_acc, out, workspace)
 
 
@@ -208,19 +234,23 @@ def bitlinear(x: torch.Tensor, packed: torch.Tensor, w_scale: torch.Tensor, N: i
         raise ValueError("x must be 2-D [M, K]")
     M = x.shape[0]
     dev = x.device
-    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=dev)
+    if out is not None:
+        _dev(out, "out")
+        y = out
+    else:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
     acc = torch.empty((M, N), dtype=torch.int32, device=dev) if want_acc else None
     xq = torch.empty((M, K), dtype=torch.int8, device=dev) if want_xq else None
     sc = torch.empty(M, dtype=torch.float32, device=dev) if want_xq else None
-    nbytes = bitlinear_workspace_bytes(M, N, K)
     stream = _stream(dev)
     if workspace is None:
-        workspace = _ws.get(dev, "bitlinear", nbytes, stream)
-    ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+        workspace = _ws.get(dev, "bitlinear", _ws_bytes("bitnet_bitlinear_workspace_bytes", M, N, K), stream)
     st = _L().bitnet_bitlinear(x.data_ptr(), _dtype_code(x), M, packed.data_ptr(), w_scale.data_ptr(), N, K,
-                               y.data_ptr(), ptr(xq), ptr(sc), ptr(acc), workspace.data_ptr(), workspace.numel(),
-                               stream)
-    _lib.check("bitnet_bitlinear", st)
+                               y.data_ptr(), xq.data_ptr() if want_xq else None,
+                               sc.data_ptr() if want_xq else None, acc.data_ptr() if want_acc else None,
+                               workspace.data_ptr(), workspace.numel(), stream)
+    if st:
+        _lib.check("bitnet_bitlinear", st)
     res = (y,)
     if want_acc:
         res += (acc,)

@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include <cudaTypedefs.h>
 
@@ -104,14 +105,23 @@ bitnet_status launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return e == cudaSuccess ? BITNET_OK : BITNET_ERR_CUDA;
 }
 
+// Dynamic shared memory already allowed per (device, kernel): the attribute
+// is set once per kernel and device, and again only for a larger size.
+std::unordered_map<const void *, size_t> g_smem_set[kMaxDevices];
+
 template <typename K>
 bitnet_status set_smem(K kernel, size_t bytes) {
-  // cudaFuncSetAttribute is cheap and per device; it is called on every
-  // launch that needs more than the default 48 KB.
   if (bytes <= 48 * 1024) return BITNET_OK;
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess
-             ? BITNET_OK
-             : BITNET_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BITNET_ERR_CUDA;
+  const void *key = reinterpret_cast<const void *>(kernel);
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_smem_set[dev].find(key);
+  if (it != g_smem_set[dev].end() && it->second >= bytes) return BITNET_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+    return BITNET_ERR_CUDA;
+  g_smem_set[dev][key] = bytes;
+  return BITNET_OK;
 }
 
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -701,8 +711,8 @@ extern "C" {
 int bitnet_w2a8_gemv_static_scratch(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
                                     const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc,
                                     cudaStream_t stream) {
-  // Validate everything bitnet_w2a8_gemv checks before the memset below is
-  // enqueued, so that a rejected call enqueues nothing.
+  // Validate everything bitnet_w2a8_gemv checks before the scratch address is
+  // looked up, so that a rejected call makes no CUDA call at all.
   if (bitnet_status s = check_gemm_args(x_q, scale, M, packed, w_scale, N, K, y, g_static_scratch_dummy))
     return s;
   if (!aligned(acc, 4)) return BITNET_ERR_ALIGNMENT;
@@ -714,9 +724,9 @@ int bitnet_w2a8_gemv_static_scratch(const int8_t *x_q, const float *scale, int64
   if (bitnet_status s = device_info(&d)) return s;
   void *scratch = nullptr;
   if (bitnet_status s = static_scratch_address(&scratch)) return s;
-  // The array keeps whatever the previous call (or an aborted one) left:
-  // the GEMV needs its scratch zero-filled on entry.
-  if (cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) return BITNET_ERR_CUDA;
+  // The array keeps whatever the previous call left.  That is harmless: the
+  // GEMV takes its workspace with any contents and zeroes, in stream order,
+  // the part it accumulates into (the stream-K partial sums and tickets).
   return bitnet_w2a8_gemv(x_q, scale, M, packed, w_scale, N, K, y, acc, scratch, need, stream);
 }
 

@@ -18,8 +18,10 @@
 //   * Every product is code * x * 2^-24 and every partial sum an integer
 //     multiple of 2^-24 below 2^22 * 2^-24, so fp32 accumulation is exact and
 //     D * 2^24 - sum_k x_q is the exact integer accumulator.
-//   * Two accumulators (256 TMEM columns) let the epilogue of one tile overlap
-//     the MMAs of the next.
+//   * With 128-token tiles two accumulators (2 x 128 TMEM columns) let the
+//     epilogue of one tile overlap the MMAs of the next; with the default
+//     256-token tiles one accumulator of 256 columns fits beside the A
+//     buffers, and the MMAs of the next tile wait for the epilogue.
 //   * When the tiles leave a last wave less than half full, those tail tiles
 //     are split by K across all CTAs (stream-K on the tail): after its whole
 //     tiles each CTA takes an equal run of (tail tile, 64-K block) units; the

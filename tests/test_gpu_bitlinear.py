@@ -41,7 +41,9 @@ def run_case(lib, oracle_mod, dev, M, N, K, dtype, seed, zero_row=False, dist="s
 # prep + tcgen05 GEMM (> 64); ragged N, K not a multiple of 512
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("M", [1, 2, 3, 16, 64, 65, 300])
-@pytest.mark.parametrize("N,K", [(300, 2560), (129, 1024), (257, 6912)])
+# K = 8192: the streaming kernel's full-register edge for one token (four
+# 16-byte chunks per lane) and the row-range kernel for two; ragged N
+@pytest.mark.parametrize("N,K", [(300, 2560), (129, 1024), (257, 6912), (777, 8192), (4097, 8192)])
 def test_bitlinear_fused(lib, oracle_mod, cuda_dev, dtype, M, N, K):
     run_case(lib, oracle_mod, cuda_dev, M, N, K, dtype, seed=M * 31 + N + K, zero_row=True)
 
