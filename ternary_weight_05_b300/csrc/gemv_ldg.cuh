@@ -18,8 +18,15 @@
 //     x_q[16q + 4b + s], b = 0..3, so masking a packed word with
 //     0x03030303 << 2s and dp4a against word s gives 4^s * sum code * x
 //     (2 integer operations per packed byte per token).
-//   * A row's 32 lane sums are combined with warp shuffles; lane m subtracts
-//     token m's sum of x_q and applies the fused dequantisation.
+//   * The plain form takes the rows of a stage four at a time, with an
+//     independent dp4a chain per row, and combines the four rows' 32 lane
+//     sums in one transpose-reduce (6 shuffles instead of 20); the lane that
+//     ends with a row's total subtracts token m's sum of x_q and applies the
+//     fused dequantisation.  The other forms combine a row's lane sums with
+//     five shuffles each.
+//   * The activations are prefetched into L2 (one bulk prefetch) before the
+//     weight stream is requested, so that the prologue's reads of x do not
+//     queue behind the weights.
 //   * Fused form (XT = float / bf16): the CTA quantises x itself in its
 //     prologue (absmax, then clamp(rint(x / s * 127)), the operations of
 //     quant_act_kernel, on 8-element halves of 16-K groups spread over all
@@ -73,6 +80,9 @@ constexpr int kLdgStages = BITNET_LDG_RING_BYTES / kLdgStageBytes;  // stages pe
 // groups in registers between the absmax and the quantisation (one read of
 // x); the host only sends shapes with M * K / 16 <= kLdgGroups * kLdgThreads.
 constexpr int kLdgGroups = 2;
+// Rows of a stage the plain form reduces together (the transpose-reduce is
+// written for four).
+constexpr int kLdgBatch = 4;
 
 constexpr int kLdgPlain = 0, kLdgSwiGLU = 1, kLdgGrouped = 2;  // kernel forms
 
@@ -195,6 +205,14 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
     for (int e = lane; e < nr * p.NG; e += 32) cp_async4(dst + e, src + e);
     cp_async_commit();
   };
+  // The activations go to L2 ahead of the weight stream.  A prefetch is only
+  // a hint (L2 stays coherent with the previous kernel's writes), so it may
+  // be issued before waiting on that kernel; the reads of x come after.
+  if (tid == 0) {
+    const void *xs = std::is_same<XT, int8_t>::value ? static_cast<const void *>(p.xq) : p.x;
+    const uint32_t xb = (uint32_t)((int64_t)p.M * p.K * sizeof(XT));
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(xs), "r"(xb) : "memory");
+  }
   if (lane == 0) {
     policy = l2_policy_evict_first();
     for (int st = 0; st < nst && st < NS; ++st) issue(st);
@@ -397,6 +415,69 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
     }
   };
 
+  // Plain form: kLdgBatch rows of a stage at once (rows b .. b + 3 of the
+  // stage at `stage`, those below nr), with independent dp4a chains per row,
+  // then one transpose-reduce over the warp: the lanes trade halves of the
+  // four row sums (xor 16, then xor 8) and finish with three butterfly
+  // steps, 6 shuffles for four rows instead of 20.  Lane group g = lane / 8
+  // ends with the totals of row b + g; lane 8 g + m writes token m's output.
+  auto rows_batch = [&](const uint8_t *stage, int b, int nr, int64_t ra) {
+    int a[kLdgBatch][MT][4];
+#pragma unroll
+    for (int r = 0; r < kLdgBatch; ++r)
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) a[r][m][s] = 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int c = lane + 32 * j;
+#pragma unroll
+      for (int r = 0; r < kLdgBatch; ++r) {
+        if (b + r >= nr) continue;  // warp-uniform: the stage's last batch may be short
+        uint4 wq = make_uint4(0u, 0u, 0u, 0u);
+        if (c < p.C) wq = lds_u128(smem_u32(stage + (size_t)(b + r) * rowb + (size_t)c * 16));
+        const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t f0 = wv[u] & 0x03030303u, f1 = wv[u] & 0x0C0C0C0Cu;
+          const uint32_t f2 = wv[u] & 0x30303030u, f3 = wv[u] & 0xC0C0C0C0u;
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            a[r][m][0] = dp4a_u8s8(f0, xr[m][j][4 * u + 0], a[r][m][0]);
+            a[r][m][1] = dp4a_u8s8(f1, xr[m][j][4 * u + 1], a[r][m][1]);
+            a[r][m][2] = dp4a_u8s8(f2, xr[m][j][4 * u + 2], a[r][m][2]);
+            a[r][m][3] = dp4a_u8s8(f3, xr[m][j][4 * u + 3], a[r][m][3]);
+          }
+        }
+      }
+    }
+    const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0;
+    const int g = (lane >> 3) & 3;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      int v[kLdgBatch];
+#pragma unroll
+      for (int r = 0; r < kLdgBatch; ++r) v[r] = a[r][m][0] + (a[r][m][1] >> 2) + (a[r][m][2] >> 4) + (a[r][m][3] >> 6);
+      // xor 16: lanes 0-15 keep rows 0, 1; lanes 16-31 rows 2, 3
+      int k0 = h16 ? v[2] : v[0], k1 = h16 ? v[3] : v[1];
+      k0 += __shfl_xor_sync(0xffffffffu, h16 ? v[0] : v[2], 16);
+      k1 += __shfl_xor_sync(0xffffffffu, h16 ? v[1] : v[3], 16);
+      // xor 8: lanes with bit 3 clear keep the even row of their pair
+      int k = h8 ? k1 : k0;
+      k += __shfl_xor_sync(0xffffffffu, h8 ? k0 : k1, 8);
+      k += __shfl_xor_sync(0xffffffffu, k, 4);
+      k += __shfl_xor_sync(0xffffffffu, k, 2);
+      k += __shfl_xor_sync(0xffffffffu, k, 1);
+      if ((lane & 7) == m && b + g < nr) {
+        const int64_t r = ra + b + g;
+        const int32_t o = k - xs[m];
+        if (p.acc) p.acc[(int64_t)m * p.N + r] = o;
+        p.y[(int64_t)m * p.N + r] = __fmul_rn((float)o, fs[m]);
+      }
+    }
+  };
+
   // grouped form: the fp32 sum over the row's groups of acc_g * scale_g, per
   // token (every lane ends with the totals).  `sc` holds the row's NG scales;
   // with `accg` non-null the per-group products go to accg[(m * N + r) * NG + g].
@@ -535,6 +616,9 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
       else cp_async_wait<0>();
       __syncwarp();
     }
+    if constexpr (FORM == kLdgPlain) {
+      for (int b = 0; b < nr; b += kLdgBatch) rows_batch(stage, b, nr, ra);
+    } else
     for (int i = 0; i < nr; ++i) {
       const int64_t r = ra + i;
       if constexpr (GR) {
