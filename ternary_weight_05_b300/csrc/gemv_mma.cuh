@@ -29,10 +29,14 @@
 //     sums are added in shared memory.  With 32 or 64 tokens the accumulators
 //     of 8 row blocks would not fit in registers: warp w then takes row block
 //     w over all K-blocks of the unit and owns its outputs alone.  At the end
-//     of a row tile's segment a tile finished inside the
-//     CTA is written directly, a tile split between CTAs is summed with int32
-//     atomics in the workspace and written by the CTA that completes it
-//     (ticket), which re-zeroes the entries.
+//     of a row tile's segment each warp stores its exact int32 partial sums
+//     into its own shared-memory slice [token][row]; the warps then add the
+//     slices output by output, consecutive threads taking consecutive rows,
+//     so that every global access below is coalesced.  A tile finished
+//     inside the CTA is written directly; a tile split between CTAs is summed
+//     with int32 atomics in the workspace and written by the CTA that
+//     completes it (ticket), which re-zeroes the entries.  The per-token sums
+//     and output scales are read into shared memory once per CTA.
 // Every wait is bounded; on expiry the CTA records the error and walks out
 // without waiting (outputs undefined, the device error word says so).
 #pragma once
@@ -50,7 +54,7 @@ struct GemvMmaParams {
   int32_t *acc;
   const int32_t *xsum;   // [M] sum of x_q per token
   const float *fscale;   // [M] w_scale * s_m / 127
-  int32_t *ws_partial;   // [NRT * 128][M], zero on entry and exit
+  int32_t *ws_partial;   // [M][NRT * 128] (row fastest), zero on entry and exit
   unsigned *ws_ticket;   // [NRT], zero on entry and exit
   int64_t N, K;
   int M;
@@ -74,10 +78,14 @@ constexpr int kMmaThreads = (kMmaWarps + 1) * 32;
 // blocks.
 template <int NT8> struct MmaCfg {
   static constexpr int ctas = NT8 == 1 ? 2 : 1;
-  static constexpr int stages = NT8 == 1 ? 3 : (NT8 == 2 ? 5 : (NT8 == 4 ? 3 : 2));
+  static constexpr int stages = NT8 == 1 ? 3 : (NT8 == 2 ? 4 : (NT8 == 4 ? 3 : 2));
   static constexpr bool wide = NT8 >= 4;
+  // partial-sum slices at a segment end: one per compute warp when the
+  // warps split K (their sums are added), one shared slice when they split rows
+  static constexpr int slices = wide ? 1 : 8;
 };
 constexpr int kMmaBar = 3;                   // named barrier of the compute warps
+constexpr int kMmaRS = 132;                  // int32 per token row of a slice (128 rows + 4: no bank conflicts)
 
 template <int NT8>
 struct GemvMmaSmem {
@@ -86,8 +94,9 @@ struct GemvMmaSmem {
   static constexpr int kBoxRows = 8 * kTok < 256 ? 8 * kTok : 256;  // TMA box limit
   static constexpr int kStage = 16384 + kBBytes;
   static constexpr int ring = 0;
-  static constexpr int red = MmaCfg<NT8>::stages * kStage;       // [128 rows][M] int32
-  static constexpr int bars = red + 128 * kTok * 4;
+  static constexpr int red = MmaCfg<NT8>::stages * kStage;  // [slices][tokens][kMmaRS] int32
+  static constexpr int toks = red + MmaCfg<NT8>::slices * kTok * kMmaRS * 4;  // xsum [64], fscale [64]
+  static constexpr int bars = toks + 512;
   static constexpr int flags = bars + 2 * MmaCfg<NT8>::stages * 8;
   static constexpr int bytes = flags + 16;
 };
@@ -102,6 +111,8 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bars);
   uint64_t *empty = full + MmaCfg<NT8>::stages;
   int32_t *red = reinterpret_cast<int32_t *>(smem + L::red);
+  int32_t *xsum_s = reinterpret_cast<int32_t *>(smem + L::toks);
+  float *fscale_s = reinterpret_cast<float *>(smem + L::toks + 256);
   volatile int *flags = reinterpret_cast<volatile int *>(smem + L::flags);  // [0] abort, [1] last CTA
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
@@ -117,7 +128,6 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
     flags[1] = 0;
     fence_mbar_init();
   }
-  for (int i = tid; i < 128 * p.M; i += kMmaThreads) red[i] = 0;
   __syncthreads();
 
   if (warp == kMmaWarps) {
@@ -159,6 +169,12 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
 
   // ---------------------------------------------------------- compute warps --
   pdl_wait_prior_grid();  // xsum / fscale come from the previous kernel
+  for (int i = tid; i < p.M; i += kMmaWarps * 32) {
+    xsum_s[i] = p.xsum[i];
+    fscale_s[i] = p.fscale[i];
+  }
+  named_barrier_sync(kMmaBar, kMmaWarps * 32);
+  const int64_t NRp = (int64_t)p.NRT * 128;  // rows of the split-tile partial sums [tokens][NRp]
   const int g = lane >> 2, t = lane & 3;
   constexpr bool kWide = MmaCfg<NT8>::wide;
   constexpr int RBN = kWide ? 1 : 8;  // row blocks in this warp's accumulators
@@ -270,47 +286,52 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
     }
 
     // ------------------------------------------------------- segment end --
-    // exact int32 partial sums into red[row][token]: added across the column
-    // warps; stored by the row-block owner in the wide form
+    // exact int32 partial sums into the warp's slice [token][row] (the
+    // fragment layout makes these stores conflict-free); the compute warps
+    // then add the slices per output, row by row, so that the outputs and
+    // the split-tile partial sums are written with coalesced accesses
+    {
+      int32_t *sl = red + (kWide ? 0 : warp) * (L::kTok * kMmaRS);
 #pragma unroll
-    for (int rb = 0; rb < RBN; ++rb)
+      for (int rb = 0; rb < RBN; ++rb)
 #pragma unroll
-      for (int nt = 0; nt < NT8; ++nt)
+        for (int nt = 0; nt < NT8; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int row = (kWide ? warp : rb) * 16 + g + ((e >> 1) << 3);
-          const int tok = nt * 8 + 2 * t + (e & 1);
-          const int v = __float2int_rn(d[rb][nt][e] * 16777216.0f);
-          d[rb][nt][e] = 0.0f;
-          if (tok < p.M) {
-            if (kWide)
-              red[row * p.M + tok] = v;
-            else if (v != 0)
-              atomicAdd(&red[row * p.M + tok], v);
+          for (int e = 0; e < 4; ++e) {
+            const int row = (kWide ? warp : rb) * 16 + g + ((e >> 1) << 3);
+            const int tok = nt * 8 + 2 * t + (e & 1);
+            const int v = __float2int_rn(d[rb][nt][e] * 16777216.0f);
+            d[rb][nt][e] = 0.0f;
+            if (tok < p.M) sl[tok * kMmaRS + row] = v;
           }
-        }
+    }
     named_barrier_sync(kMmaBar, kMmaWarps * 32);
     const bool whole = (c0 == 0) && (nch == p.NCH);
     const int entries = 128 * p.M;
+    auto total_of = [&](int row, int tok) {
+      int v = 0;
+#pragma unroll
+      for (int sl = 0; sl < MmaCfg<NT8>::slices; ++sl) v += red[(sl * L::kTok + tok) * kMmaRS + row];
+      return v;
+    };
+    auto write_out = [&](int64_t n, int tok, int32_t total) {
+      const int32_t o = total - xsum_s[tok];
+      if (p.acc) p.acc[(int64_t)tok * p.N + n] = o;
+      p.y[(int64_t)tok * p.N + n] = __fmul_rn((float)o, fscale_s[tok]);
+    };
     if (whole) {
       for (int i = tid; i < entries; i += kMmaWarps * 32) {
-        const int row = i / p.M, tok = i % p.M;
+        const int row = i & 127, tok = i >> 7;
         const int64_t n = (int64_t)r * 128 + row;
-        const int32_t v = red[i];
-        red[i] = 0;
-        if (n < p.N) {
-          const int32_t o = v - __ldg(p.xsum + tok);
-          if (p.acc) p.acc[(int64_t)tok * p.N + n] = o;
-          p.y[(int64_t)tok * p.N + n] = __fmul_rn((float)o, __ldg(p.fscale + tok));
-        }
+        const int32_t v = total_of(row, tok);
+        if (n < p.N) write_out(n, tok, v);
       }
     } else {
       for (int i = tid; i < entries; i += kMmaWarps * 32) {
-        const int row = i / p.M, tok = i % p.M;
+        const int row = i & 127, tok = i >> 7;
         const int64_t n = (int64_t)r * 128 + row;
-        const int32_t v = red[i];
-        red[i] = 0;
-        if (n < p.N && v != 0) atomicAdd(&p.ws_partial[n * p.M + tok], v);
+        const int32_t v = total_of(row, tok);
+        if (n < p.N && v != 0) atomicAdd(&p.ws_partial[(int64_t)tok * NRp + n], v);
       }
       __threadfence();  // partial sums visible before the ticket
       named_barrier_sync(kMmaBar, kMmaWarps * 32);
@@ -321,13 +342,26 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
       named_barrier_sync(kMmaBar, kMmaWarps * 32);
       if (flags[1]) {
         __threadfence();
-        for (int i = tid; i < entries; i += kMmaWarps * 32) {
-          const int row = i / p.M, tok = i % p.M;
-          const int64_t n = (int64_t)r * 128 + row;
-          if (n < p.N) {
-            const int32_t o = atomicExch(&p.ws_partial[n * p.M + tok], 0) - __ldg(p.xsum + tok);
-            if (p.acc) p.acc[(int64_t)tok * p.N + n] = o;
-            p.y[(int64_t)tok * p.N + n] = __fmul_rn((float)o, __ldg(p.fscale + tok));
+        // eight independent loads in flight per thread, then their stores:
+        // a load placed after a store that may alias would wait a whole L2
+        // round trip per output
+        constexpr int kU = 8;
+        for (int i0 = tid; i0 < entries; i0 += kU * kMmaWarps * 32) {
+          int32_t v[kU];
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            const int i = i0 + k * kMmaWarps * 32;
+            const int64_t n = (int64_t)r * 128 + (i & 127);
+            v[k] = (i < entries && n < p.N) ? __ldcg(p.ws_partial + (int64_t)(i >> 7) * NRp + n) : 0;
+          }
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            const int i = i0 + k * kMmaWarps * 32;
+            const int64_t n = (int64_t)r * 128 + (i & 127);
+            if (i < entries && n < p.N) {
+              p.ws_partial[(int64_t)(i >> 7) * NRp + n] = 0;  // leave the partial sums zero for the next call
+              write_out(n, i >> 7, v[k]);
+            }
           }
         }
         if (tid == 0) atomicExch(&p.ws_ticket[r], 0u);
