@@ -177,6 +177,59 @@ int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed,
                      int64_t N, int64_t K, float *y, int8_t *x_q, float *scale, int32_t *acc,
                      void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * bitnet_rmsnorm_quant_act -- RMSNorm, then the per-token absmax int8
+ * quantisation of the normalised activations: the input side of a BitLinear
+ * inside the BitTransformer block of [Deep-dive] §3.1 (the block applies an
+ * RMSNorm before the gate/up projections, in fp32 per §6.5), followed by the
+ * absmax quantisation of §2.2 applied to h instead of x.
+ *
+ * Per token m: S = sum_k x[m,k]^2 in fp64 (each square exact), ms =
+ * fl32(S / K), r = fl(1 / fl(sqrt(fl(ms + eps)))), h[k] = fl(fl(x[m,k] * r)
+ * * g[k]) (fl(x[m,k] * r) when g is NULL), then scale[m] = max(max_k |h|,
+ * 1e-8) and x_q = clamp(rint(fl(fl(h / s) * 127)), -127, 127).  The fp64 sum
+ * is a tree over the token's threads, so S may differ from another
+ * summation order by at most (K - 1) * 2^-53 * S; ms can then be the
+ * neighbouring fp32 value only when S / K lies that close to a rounding
+ * boundary.
+ *
+ *   x        device, [M, K] row-major, BITNET_F32 or BITNET_BF16, 16-byte aligned.
+ *   g        device, [K] float RMSNorm weight (16-byte aligned), or NULL for ones.
+ *   eps      finite, >= 0 (nn.RMSNorm's fp32 default is 2^-23).
+ *   x_q      device, [M, K] int8 out (8-byte aligned).
+ *   scale    device, [M] float out: absmax of h.
+ *   h        device, [M, K] float out (16-byte aligned), or NULL.
+ *   ms       device, [M] float out: the mean squares, or NULL.
+ * Errors: INVALID_ARG (null x / x_q / scale, dtype, eps), SHAPE (M, K <= 0,
+ * K % 8 != 0), ALIGNMENT, UNSUPPORTED, CUDA.
+ */
+int bitnet_rmsnorm_quant_act(const void *x, int dtype, int64_t M, int64_t K, const float *g, float eps,
+                             int8_t *x_q, float *scale, float *h, float *ms, cudaStream_t stream);
+
+/*
+ * bitnet_bitlinear_rmsnorm -- RMSNorm in front of the BitLinear forward:
+ * y = BitLinear(h) with h = RMSNorm(x) formed as bitnet_rmsnorm_quant_act
+ * forms it ([Deep-dive] §3.1, §5.3 fusion).  For M >= 3 (K % 64 == 0,
+ * 512 <= K <= 65536) one prep kernel computes the RMSNorm, the absmax
+ * quantisation and the tensor-core operand layout, followed by the GEMV
+ * (M <= 64) or GEMM kernel; otherwise bitnet_rmsnorm_quant_act runs first,
+ * then the int8 GEMV / GEMM.  Results are bit-identical between the two
+ * routes.
+ *
+ *   x, g, eps   as bitnet_rmsnorm_quant_act.
+ *   packed, w_scale, N, K, y, acc: as bitnet_w2a8_gemv.
+ *   x_q, scale  device outs (x_q 8-byte aligned), or NULL.
+ *   ms          device, [M] float out (mean squares), or NULL.
+ *   workspace   device, >= bitnet_bitlinear_workspace_bytes(M, N, K) bytes,
+ *               256-byte aligned, any contents.
+ * Errors: INVALID_ARG, SHAPE (also K % 8 != 0), ALIGNMENT, WORKSPACE,
+ * UNSUPPORTED, CUDA.
+ */
+int bitnet_bitlinear_rmsnorm(const void *x, int dtype, int64_t M, const float *g, float eps,
+                             const uint8_t *packed, const float *w_scale, int64_t N, int64_t K, float *y,
+                             int8_t *x_q, float *scale, float *ms, int32_t *acc, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
 /* Workspace bytes bitnet_bitlinear_swiglu needs. */
 size_t bitnet_bitlinear_swiglu_workspace_bytes(int64_t M, int64_t I, int64_t K);
 

@@ -21,6 +21,7 @@ __all__ = [
     "BitnetError", "pack_weights", "quant_act", "w2a8_gemv", "w2a8_gemm", "bitlinear", "bitlinear_workspace_bytes",
     "pack_workspace_bytes", "gemv_workspace_bytes", "gemm_workspace_bytes", "check_device_error",
     "set_pdl", "GEMV_MAX_M", "library_path", "w2a8_gemv_static_scratch", "GEMV_STATIC_SCRATCH_BYTES",
+    "rmsnorm_quant_act", "bitlinear_rmsnorm", "RMS_EPS",
 ]
 
 GEMV_MAX_M = 64
@@ -256,6 +257,75 @@ def bitlinear(x: torch.Tensor, packed: torch.Tensor, w_scale: torch.Tensor, N: i
         res += (acc,)
     if want_xq:
         res += (xq, sc)
+    return res[0] if len(res) == 1 else res
+
+
+RMS_EPS = 2.0 ** -23  # nn.RMSNorm's default eps for fp32
+
+
+def rmsnorm_quant_act(x: torch.Tensor, g=None, eps: float = RMS_EPS, want_h: bool = False, want_ms: bool = False):
+    """RMSNorm of x [M, K] (bf16/fp32, K % 8 == 0) with weight g [K] (None:
+    ones), then per-token absmax int8 quantisation of the normalised h.
+
+    Returns (x_q int8 [M, K], scale f32 [M]) and, if asked, h f32 [M, K] and
+    the mean squares f32 [M]."""
+    _dev(x, "x")
+    if g is not None:
+        _dev(g, "g")
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    M, K = x.shape
+    dev = x.device
+    xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+    sc = torch.empty(M, dtype=torch.float32, device=dev)
+    h = torch.empty((M, K), dtype=torch.float32, device=dev) if want_h else None
+    ms = torch.empty(M, dtype=torch.float32, device=dev) if want_ms else None
+    ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+    st = _L().bitnet_rmsnorm_quant_act(x.data_ptr(), _dtype_code(x), M, K, ptr(g), eps, xq.data_ptr(), sc.data_ptr(),
+                                       ptr(h), ptr(ms), _stream(dev))
+    _lib.check("bitnet_rmsnorm_quant_act", st)
+    res = (xq, sc)
+    if want_h:
+        res += (h,)
+    if want_ms:
+        res += (ms,)
+    return res
+
+
+def bitlinear_rmsnorm(x: torch.Tensor, g, packed: torch.Tensor, w_scale: torch.Tensor, N: int, K: int,
+                      eps: float = RMS_EPS, want_acc: bool = False, want_xq: bool = False, want_ms: bool = False,
+                      out=None, workspace=None):
+    """BitLinear forward on RMSNorm(x): y fp32 [M, N]; g [K] fp32 or None;
+    with want_acc the exact int32 products, want_xq (x_q, scale), want_ms the
+    mean squares."""
+    for t, nm in ((x, "x"), (packed, "packed"), (w_scale, "w_scale")):
+        _dev(t, nm)
+    if g is not None:
+        _dev(g, "g")
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    M = x.shape[0]
+    dev = x.device
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=dev)
+    acc = torch.empty((M, N), dtype=torch.int32, device=dev) if want_acc else None
+    xq = torch.empty((M, K), dtype=torch.int8, device=dev) if want_xq else None
+    sc = torch.empty(M, dtype=torch.float32, device=dev) if want_xq else None
+    ms = torch.empty(M, dtype=torch.float32, device=dev) if want_ms else None
+    stream = _stream(dev)
+    if workspace is None:
+        workspace = _ws.get(dev, "bitlinear", _ws_bytes("bitnet_bitlinear_workspace_bytes", M, N, K), stream)
+    ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+    st = _L().bitnet_bitlinear_rmsnorm(x.data_ptr(), _dtype_code(x), M, ptr(g), eps, packed.data_ptr(),
+                                       w_scale.data_ptr(), N, K, y.data_ptr(), ptr(xq), ptr(sc), ptr(ms), ptr(acc),
+                                       workspace.data_ptr(), workspace.numel(), stream)
+    _lib.check("bitnet_bitlinear_rmsnorm", st)
+    res = (y,)
+    if want_acc:
+        res += (acc,)
+    if want_xq:
+        res += (xq, sc)
+    if want_ms:
+        res += (ms,)
     return res[0] if len(res) == 1 else res
 
 

@@ -22,6 +22,7 @@
 #include "grouped.cuh"
 #include "pack.cuh"
 #include "quant_act.cuh"
+#include "rmsnorm.cuh"
 
 using namespace bitnet;
 
@@ -438,6 +439,9 @@ bitnet_status static_scratch_address(void **out) {
 bitnet_status launch_gemm_tc(uint32_t *xb, int32_t *xsum, float *fscale, int64_t M, const uint8_t *packed, int64_t N,
                              int64_t K, float *y, int32_t *acc, const GemmSplit &sp, uint8_t *part,
                              const DeviceInfo *d, cudaStream_t stream);
+bitnet_status bitlinear_tc(const void *x, bool bf, int64_t M, const uint8_t *packed, const float *w_scale, int64_t N,
+                           int64_t K, float *y, int8_t *x_q, float *scale, int32_t *acc, void *workspace,
+                           size_t workspace_bytes, const DeviceInfo *d, const PrepNorm &norm, cudaStream_t stream);
 
 // Stream-K split of the GEMM's tail tiles when the workspace holds its
 // partial sums (sized for 148 SMs), else whole tiles only.
@@ -764,8 +768,33 @@ int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed,
                                                 stream)
               : launch_gemv_rows<float>(nullptr, nullptr, x, x_q, scale, M, packed, w_scale, N, K, y, acc, d, stream);
   }
+  if (fused && K <= kTensorMaxK)
+    return bitlinear_tc(x, bf, M, packed, w_scale, N, K, y, x_q, scale, acc, workspace, workspace_bytes, d,
+                        PrepNorm{nullptr, -1.0f, nullptr}, stream);
+  // Unfused: quantise into the caller's buffers or the workspace tail, then
+  // the GEMV / GEMM entry points.
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  if (fused && K <= kTensorMaxK) {
+  const size_t base = M <= BITNET_GEMV_MAX_M ? plan_gemv(M, N, K, d->sms).ws_bytes : gemm_workspace_bytes(M, N, K);
+  int8_t *xq_buf = x_q ? x_q : reinterpret_cast<int8_t *>(ws + base);
+  float *s_buf = scale ? scale : reinterpret_cast<float *>(ws + base + (((size_t)M * (size_t)K + 255) & ~(size_t)255));
+  if (int st = bitnet_quant_act(x, dtype, M, K, xq_buf, s_buf, stream)) return st;
+  if (M <= BITNET_GEMV_MAX_M)
+    return bitnet_w2a8_gemv(xq_buf, s_buf, M, packed, w_scale, N, K, y, acc, workspace, base, stream);
+  return bitnet_w2a8_gemm(xq_buf, s_buf, M, packed, w_scale, N, K, y, acc, workspace, base, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The fused BitLinear on the tensor cores (M >= 3): one prep kernel
+// quantises x (after an RMSNorm when norm.eps >= 0) straight into the
+// operand layout, then the GEMV (M <= 64) or the GEMM.
+bitnet_status bitlinear_tc(const void *x, bool bf, int64_t M, const uint8_t *packed, const float *w_scale, int64_t N,
+                           int64_t K, float *y, int8_t *x_q, float *scale, int32_t *acc, void *workspace,
+                           size_t workspace_bytes, const DeviceInfo *d, const PrepNorm &norm, cudaStream_t stream) {
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  {
     uint32_t *xb;
     int32_t *xsum;
     float *fscale;
@@ -789,20 +818,66 @@ int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed,
     bitnet_status st =
         bf ? launch(fused_prep_kernel<__nv_bfloat16>, pgrid, dim3(256), 0, stream,
                     static_cast<const __nv_bfloat16 *>(x), w_scale, K, xb, xsum, fscale, x_q, scale, M, zero, zero_n16,
-                    trows)
+                    trows, norm)
            : launch(fused_prep_kernel<float>, pgrid, dim3(256), 0, stream, static_cast<const float *>(x), w_scale, K,
-                    xb, xsum, fscale, x_q, scale, M, zero, zero_n16, trows);
+                    xb, xsum, fscale, x_q, scale, M, zero, zero_n16, trows, norm);
     if (st) return st;
     if (M <= BITNET_GEMV_MAX_M)
       return launch_gemv_mma(nullptr, nullptr, M, packed, w_scale, N, K, y, acc, workspace, pl, d, stream);
     return launch_gemm_tc(xb, xsum, fscale, M, packed, N, K, y, acc, sp, part, d, stream);
   }
-  // Unfused: quantise into the caller's buffers or the workspace tail, then
-  // the GEMV / GEMM entry points.
+}
+
+}  // namespace
+
+extern "C" {
+
+int bitnet_rmsnorm_quant_act(const void *x, int dtype, int64_t M, int64_t K, const float *g, float eps, int8_t *x_q,
+                             float *scale, float *h, float *ms, cudaStream_t stream) {
+  if (!x || !x_q || !scale) return BITNET_ERR_INVALID_ARG;
+  if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.0f) return BITNET_ERR_INVALID_ARG;
+  if (M <= 0 || K <= 0 || K % 8 != 0 || M > kMaxElems / K || M > 0x7fffffff) return BITNET_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(g, 16) || !aligned(x_q, 8) || !aligned(scale, 4) || !aligned(h, 16) ||
+      !aligned(ms, 4))
+    return BITNET_ERR_ALIGNMENT;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
+  return dtype == BITNET_F32
+             ? launch(rmsnorm_quant_kernel<float>, dim3((unsigned)M), dim3(256), 0, stream,
+                      static_cast<const float *>(x), K, g, eps, x_q, scale, h, ms)
+             : launch(rmsnorm_quant_kernel<__nv_bfloat16>, dim3((unsigned)M), dim3(256), 0, stream,
+                      static_cast<const __nv_bfloat16 *>(x), K, g, eps, x_q, scale, h, ms);
+}
+
+int bitnet_bitlinear_rmsnorm(const void *x, int dtype, int64_t M, const float *g, float eps, const uint8_t *packed,
+                             const float *w_scale, int64_t N, int64_t K, float *y, int8_t *x_q, float *scale,
+                             float *ms, int32_t *acc, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!x || !packed || !w_scale || !y) return BITNET_ERR_INVALID_ARG;
+  if (dtype != BITNET_F32 && dtype != BITNET_BF16) return BITNET_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.0f) return BITNET_ERR_INVALID_ARG;
+  if (M <= 0 || !shape_ok(N, K) || K % 8 != 0 || M > kMaxElems / K || M > kMaxElems / N) return BITNET_ERR_SHAPE;
+  if (N > 0x7fffffff || K > 0x7fffffff || M > 0x7fffffff) return BITNET_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(g, 16) || !aligned(w_scale, 4) || !aligned(y, 4) || !aligned(scale, 4) ||
+      !aligned(ms, 4) || !aligned(acc, 4) || !aligned(x_q, 8))
+    return BITNET_ERR_ALIGNMENT;
+  const size_t need = bitnet_bitlinear_workspace_bytes(M, N, K);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return BITNET_ERR_WORKSPACE;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
+  const bool bf = dtype == BITNET_BF16;
+  // M >= 3 on the tensor cores: the RMSNorm, the quantisation and the
+  // operand layout in one prep kernel, then the GEMV / GEMM
+  if (M >= 3 && K % 64 == 0 && K >= kStageK && K <= kTensorMaxK && aligned(packed, 16) && aligned(x_q, 16))
+    return bitlinear_tc(x, bf, M, packed, w_scale, N, K, y, x_q, scale, acc, workspace, workspace_bytes, d,
+                        PrepNorm{g, eps, ms}, stream);
+  // otherwise: RMSNorm + quantisation into int8 (the caller's buffers or the
+  // workspace tail), then the GEMV / GEMM entry points
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
   const size_t base = M <= BITNET_GEMV_MAX_M ? plan_gemv(M, N, K, d->sms).ws_bytes : gemm_workspace_bytes(M, N, K);
   int8_t *xq_buf = x_q ? x_q : reinterpret_cast<int8_t *>(ws + base);
   float *s_buf = scale ? scale : reinterpret_cast<float *>(ws + base + (((size_t)M * (size_t)K + 255) & ~(size_t)255));
-  if (int st = bitnet_quant_act(x, dtype, M, K, xq_buf, s_buf, stream)) return st;
+  if (int st = bitnet_rmsnorm_quant_act(x, dtype, M, K, g, eps, xq_buf, s_buf, nullptr, ms, stream)) return st;
   if (M <= BITNET_GEMV_MAX_M)
     return bitnet_w2a8_gemv(xq_buf, s_buf, M, packed, w_scale, N, K, y, acc, workspace, base, stream);
   return bitnet_w2a8_gemm(xq_buf, s_buf, M, packed, w_scale, N, K, y, acc, workspace, base, stream);

@@ -38,6 +38,7 @@
 
 #include "common.cuh"
 #include "quant_act.cuh"
+#include "rmsnorm.cuh"
 
 namespace bitnet {
 
@@ -311,12 +312,22 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const int8_t *__restrict
 // quant_act_kernel) straight into the B layout, the per-token sum of x_q and
 // the output scale.  Optionally also writes x_q and s.  One CTA per token;
 // K % 16 == 0 and 16-byte aligned rows (checked on the host).
+//
+// With an RMSNorm (`norm` non-null: norm->g, norm->eps) the kernel first
+// forms the token's normalisation factor r (rmsnorm.cuh) and quantises
+// h = fl(fl(x * r) * g) instead of x.
+struct PrepNorm {
+  const float *g;  // [K] or nullptr (a weight of ones)
+  float eps;
+  float *ms_out;   // [M] mean squares, or nullptr
+};
+
 template <typename T>
 __global__ void __launch_bounds__(256)
     fused_prep_kernel(const T *__restrict__ x, const float *__restrict__ w_scale, int64_t K,
                       uint32_t *__restrict__ xb, int32_t *__restrict__ xsum, float *__restrict__ fscale,
                       int8_t *__restrict__ xq_out, float *__restrict__ scale_out, int64_t M, uint4 *zero,
-                      int64_t zero_n16, int TR) {
+                      int64_t zero_n16, int TR, const PrepNorm norm) {
   pdl_launch_dependents();
   pdl_wait_prior_grid();
   const int64_t rows = M > TR ? M : TR;
@@ -330,12 +341,17 @@ __global__ void __launch_bounds__(256)
   }
   __shared__ float redf[8];
   __shared__ int red[8];
+  __shared__ double redd[8];
   const int64_t m = blockIdx.x;
   const T *row = x + m * K;
+  const bool rms = norm.eps >= 0.0f;  // a negative eps marks "no RMSNorm"
+  const float r =
+      rms ? rms_factor(row, K, norm.eps, redd, (norm.ms_out && threadIdx.x == 0) ? norm.ms_out + m : nullptr) : 1.0f;
   float amax = 0.0f;
   for (int64_t k = (int64_t)threadIdx.x * 8; k < K; k += 256 * 8) {
     float v[8];
     load8(row + k, v);
+    if (rms) rms_apply8(v, r, norm.g, k);
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
   }
@@ -346,6 +362,10 @@ __global__ void __launch_bounds__(256)
     float f[8], g[8];
     load8(row + q * 16, f);
     load8(row + q * 16 + 8, g);
+    if (rms) {
+      rms_apply8(f, r, norm.g, q * 16);
+      rms_apply8(g, r, norm.g, q * 16 + 8);
+    }
     int8_t v[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {

@@ -121,6 +121,35 @@ def test_bitlinear_validation(clib):
     assert call(work=FAKE + 16) == WORKSPACE  # not 256-byte aligned
 
 
+def test_rmsnorm_validation(clib):
+    def quant(x=FAKE, dt=1, M=1, K=64, g=None, eps=2.0 ** -23, xq=FAKE, s=FAKE, h=None):
+        return clib.bitnet_rmsnorm_quant_act(x, dt, M, K, g, eps, xq, s, h, None, None)
+
+    assert quant(x=None) == INVALID_ARG
+    assert quant(s=None) == INVALID_ARG
+    assert quant(dt=5) == INVALID_ARG
+    assert quant(eps=-1.0) == INVALID_ARG
+    assert quant(eps=float("nan")) == INVALID_ARG
+    assert quant(M=0) == SHAPE
+    assert quant(K=12) == SHAPE  # K % 8 != 0
+    assert quant(x=FAKE + 8) == ALIGNMENT
+    assert quant(g=FAKE + 4) == ALIGNMENT
+    assert quant(h=FAKE + 4) == ALIGNMENT
+    nb = clib.bitnet_bitlinear_workspace_bytes(2, 8, 64)
+
+    def bl(x=FAKE, g=None, eps=2.0 ** -23, K=64, y=FAKE, work=FAKE, wb=nb):
+        return clib.bitnet_bitlinear_rmsnorm(x, 1, 2, g, eps, FAKE, FAKE, 8, K, y, None, None, None, None, work, wb,
+                                             None)
+
+    assert bl(x=None) == INVALID_ARG
+    assert bl(y=None) == INVALID_ARG
+    assert bl(eps=float("inf")) == INVALID_ARG
+    assert bl(K=60) == SHAPE  # K % 8 != 0
+    assert bl(g=FAKE + 8) == ALIGNMENT
+    assert bl(work=None) == WORKSPACE
+    assert bl(wb=nb - 1) == WORKSPACE
+
+
 def test_bitlinear_swiglu_validation(clib):
     nb = clib.bitnet_bitlinear_swiglu_workspace_bytes(2, 8, 64)
     # the fallback's two [M, I] fp32 outputs come on top of the BitLinear's
@@ -298,6 +327,10 @@ def test_injected_cuda_failure_reaches_every_caller(clib):
         "fake_quant": lambda: clib.bitnet_bitlinear_fake_quant(FAKE, 0, FAKE, 1, 2, 8, 64, 1.0, 1e-8, None, FAKE,
                                                                None, None, None, None, None, FAKE, nb_fq, None),
         "selftest": lambda: clib.bitnet_selftest_wait_timeout(2_000_000, None),
+        "rmsnorm_quant": lambda: clib.bitnet_rmsnorm_quant_act(FAKE, 1, 2, 64, None, 2.0 ** -23, FAKE, FAKE, None,
+                                                               None, None),
+        "bitlinear_rmsnorm": lambda: clib.bitnet_bitlinear_rmsnorm(FAKE, 1, 2, FAKE, 2.0 ** -23, FAKE, FAKE, 8, 64,
+                                                                   FAKE, None, None, None, None, FAKE, nb_bl, None),
     }
     n = len(calls) + 3
     assert clib.bitnet_test_inject_cuda_failures(n) == 0
