@@ -625,18 +625,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int64_t tok0 = (int64_t)tt * kGemmTok + cb * 32;
             const int32_t xs_l = tok0 + lane < p.M ? __ldg(p.xsum + tok0 + lane) : 0;
             const float fs_l = tok0 + lane < p.M ? __ldg(p.fscale + tok0 + lane) : 0.0f;
+            // all 32 partial sums in flight at once, then their stores (a
+            // load after a store that may alias would wait a whole L2 round
+            // trip per output)
+#pragma unroll 1
+            for (int j0 = 0; j0 < 32; j0 += 8) {
+              int32_t total[8];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int32_t xs = __shfl_sync(0xffffffffu, xs_l, j);
-              const float fs = __shfl_sync(0xffffffffu, fs_l, j);
-              int32_t *pp = part + (size_t)(cb * 32 + j) * kGemmRows + row;
-              const int32_t total = __ldcg(pp);
-              *pp = 0;
-              const int64_t tok = tok0 + j;
-              if (n < p.N && tok < p.M) {
-                const int32_t v = total - xs;
-                if (p.acc) p.acc[tok * p.N + n] = v;
-                p.y[tok * p.N + n] = __fmul_rn((float)v, fs);
+              for (int j = 0; j < 8; ++j) total[j] = __ldcg(part + (size_t)(cb * 32 + j0 + j) * kGemmRows + row);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int32_t xs = __shfl_sync(0xffffffffu, xs_l, j0 + j);
+                const float fs = __shfl_sync(0xffffffffu, fs_l, j0 + j);
+                part[(size_t)(cb * 32 + j0 + j) * kGemmRows + row] = 0;
+                const int64_t tok = tok0 + j0 + j;
+                if (n < p.N && tok < p.M) {
+                  const int32_t v = total[j] - xs;
+                  if (p.acc) p.acc[tok * p.N + n] = v;
+                  p.y[tok * p.N + n] = __fmul_rn((float)v, fs);
+                }
               }
             }
           }
