@@ -39,11 +39,11 @@ PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 
-# DRAM bytes (read + write) per launch of the dominant kernel, averaged over a
-# step, from one ncu capture of this kernel version (the launch list in
-# profiles/launches_2b_decode_fused_step.md); a step of another shape or
-# another kernel version reports null instead.
-MEASURED_TRAFFIC = {("2b-decode", 1, True, 0): 3.360e6}
+# DRAM bytes (read + write) per launch of the dominant kernel from one ncu
+# capture of this kernel version (profiles/gemv_ldg_kernel_100b_stream_m1.md,
+# the same 28672 x 8192 launch the default step makes); a step of another
+# shape or another kernel version reports null instead.
+MEASURED_TRAFFIC = {("100b-stream", 1, True, 0): 58.799e6}
 
 # Output rows of each prefill matrix the CPU oracle computes per sample pass
 # (all 2048 tokens, the whole K), to keep its timing bounded.
