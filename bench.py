@@ -467,10 +467,11 @@ def run_native(args):
     # kernels per BitLinear: fused M <= 2: 1; fused M >= 3: prep + tensor-core GEMV;
     # unfused: quant_act (+ prep for M >= 3) + GEMV
     if G:
-        # fused M <= 2: one streaming kernel; otherwise quant_act + the generic grouped kernel
+        # fused M <= 2: one streaming kernel; M >= 3 (fused or not): the prep
+        # kernel + the grouped tensor-core GEMV (64 tokens per chunk)
         per_layer = 1 if (fused and M <= 2) else 2
-        kname = ("gemv_ldg_kernel grouped form" if M <= 2 else "grouped_generic_kernel") + \
-            (" (fused quant)" if fused and M <= 2 else "")
+        kname = ("gemv_ldg_kernel grouped form" if M <= 2 else "gemv_mma_grouped_kernel (+prep)") + \
+            (" (fused quant)" if fused else "")
     else:
         per_layer = (1 if M <= 2 else 2) if fused else (2 if M <= 2 else 3)
         kname = ("gemv_ldg_kernel" if M <= 2 else "gemv_mma_kernel (+prep)") + (" (fused quant)" if fused else "")

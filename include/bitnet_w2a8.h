@@ -324,7 +324,11 @@ size_t bitnet_bitlinear_grouped_workspace_bytes(int64_t M, int64_t K);
  *   x        device, [M, K], BITNET_F32 or BITNET_BF16.
  *   x_q, scale: device outs ([M, K] int8, [M] float), or NULL.
  *   workspace device, >= bitnet_bitlinear_grouped_workspace_bytes(M, K),
- *            256-byte aligned, any contents.
+ *            256-byte aligned, any contents.  With at least
+ *            bitnet_grouped_workspace_bytes(M, N, K, G) bytes, three or more
+ *            tokens run on the tensor cores (as bitnet_w2a8_grouped_ws: one
+ *            prep kernel quantises into the operand layout and forms the
+ *            group sums, then the grouped GEMV, 64 tokens at a time).
  *   other arguments as bitnet_w2a8_grouped.
  * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA.
  */
@@ -332,6 +336,30 @@ int bitnet_bitlinear_grouped(const void *x, int dtype, int64_t M, const uint8_t 
                              const float *w_scale, int64_t N, int64_t K, int64_t G, float *y,
                              int8_t *x_q, float *scale, int32_t *acc_g, void *workspace,
                              size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes of bitnet_w2a8_grouped_ws, and of bitnet_bitlinear_grouped
+ * on its tensor-core path (0 for shapes the group calls reject). */
+size_t bitnet_grouped_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t G);
+
+/*
+ * bitnet_w2a8_grouped_ws -- bitnet_w2a8_grouped (same operation, arguments
+ * and error bound, [Deep-dive] §4.3 group-wise scales) with a workspace, so
+ * that three or more tokens run on the tensor cores: G in {64, 128, 256,
+ * 512} or a single group per row of at most 512 weights (K % G == 0, K % 64
+ * == 0, 512 <= K <= 65536, at most 1024 groups per row and
+ * 64 * (K / G) * 4 <= 16 KB), x_q and packed 16-byte aligned.  Per 64
+ * tokens, a prep kernel writes the fp16 operand layout and each token's sum
+ * of x_q per group, then the mma.sync GEMV accumulates each group exactly,
+ * stores acc_g if asked and adds acc_g * w_scale[n, g] into F with one fp32
+ * FMA per group.  Other shapes (and M <= 2) take bitnet_w2a8_grouped's
+ * kernels.
+ *   workspace device, >= bitnet_grouped_workspace_bytes(M, N, K, G) bytes,
+ *             256-byte aligned, any contents.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA.
+ */
+int bitnet_w2a8_grouped_ws(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
+                           const float *w_scale, int64_t N, int64_t K, int64_t G, float *y, int32_t *acc_g,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Workspace bytes bitnet_bitlinear_fake_quant needs. */
 size_t bitnet_bitlinear_fake_quant_workspace_bytes(int64_t M, int64_t N, int64_t K);

@@ -21,7 +21,8 @@ __all__ = [
     "BitnetError", "pack_weights", "quant_act", "w2a8_gemv", "w2a8_gemm", "bitlinear", "bitlinear_workspace_bytes",
     "pack_workspace_bytes", "gemv_workspace_bytes", "gemm_workspace_bytes", "check_device_error",
     "set_pdl", "GEMV_MAX_M", "library_path", "w2a8_gemv_static_scratch", "GEMV_STATIC_SCRATCH_BYTES",
-    "rmsnorm_quant_act", "bitlinear_rmsnorm", "RMS_EPS",
+    "rmsnorm_quant_act", "bitlinear_rmsnorm", "RMS_EPS", "w2a8_grouped", "bitlinear_grouped", "pack_weights_grouped",
+    "grouped_workspace_bytes",
 ]
 
 GEMV_MAX_M = 64
@@ -395,18 +396,30 @@ def pack_weights_grouped(W: torch.Tensor, G: int, alpha: float = 1.0, eps: float
     return packed, w_scale, absmean
 
 
-def w2a8_grouped(x_q, scale, packed, w_scale, N: int, K: int, G: int, want_acc: bool = False, out=None):
+def grouped_workspace_bytes(M: int, N: int, K: int, G: int) -> int:
+    """Bytes of device scratch the group-scaled calls need on their tensor-core path."""
+    return int(_L().bitnet_grouped_workspace_bytes(M, N, K, G))
+
+
+def w2a8_grouped(x_q, scale, packed, w_scale, N: int, K: int, G: int, want_acc: bool = False, out=None,
+                 workspace=None):
     """Ternary matmul with group scales w_scale [N, K//G], any M: y fp32 [M, N]
-    (and the exact per-group int32 products [M, N, K//G] if asked)."""
+    (and the exact per-group int32 products [M, N, K//G] if asked).  Three or
+    more tokens run on the tensor cores when the shape allows (a workspace
+    is taken from the cache unless given)."""
     for t, nm in ((x_q, "x_q"), (scale, "scale"), (packed, "packed"), (w_scale, "w_scale")):
         _dev(t, nm)
     M = x_q.shape[0]
     dev = x_q.device
     y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=dev)
     acc = torch.empty((M, N, K // G), dtype=torch.int32, device=dev) if want_acc else None
-    st = _L().bitnet_w2a8_grouped(x_q.data_ptr(), scale.data_ptr(), M, packed.data_ptr(), w_scale.data_ptr(), N, K,
-                                  G, y.data_ptr(), acc.data_ptr() if acc is not None else None, _stream(dev))
-    _lib.check("bitnet_w2a8_grouped", st)
+    stream = _stream(dev)
+    if workspace is None:
+        workspace = _ws.get(dev, "grouped", _ws_bytes("bitnet_grouped_workspace_bytes", M, N, K, G), stream)
+    st = _L().bitnet_w2a8_grouped_ws(x_q.data_ptr(), scale.data_ptr(), M, packed.data_ptr(), w_scale.data_ptr(), N,
+                                     K, G, y.data_ptr(), acc.data_ptr() if acc is not None else None,
+                                     workspace.data_ptr(), workspace.numel(), stream)
+    _lib.check("bitnet_w2a8_grouped_ws", st)
     return (y, acc) if want_acc else y
 
 
@@ -424,10 +437,9 @@ def bitlinear_grouped(x: torch.Tensor, packed: torch.Tensor, w_scale: torch.Tens
     acc = torch.empty((M, N, K // G), dtype=torch.int32, device=dev) if want_acc else None
     xq = torch.empty((M, K), dtype=torch.int8, device=dev) if want_xq else None
     sc = torch.empty(M, dtype=torch.float32, device=dev) if want_xq else None
-    nbytes = bitlinear_grouped_workspace_bytes(M, K)
     stream = _stream(dev)
     if workspace is None:
-        workspace = _ws.get(dev, "bitlinear_grouped", nbytes, stream)
+        workspace = _ws.get(dev, "bitlinear_grouped", _ws_bytes("bitnet_grouped_workspace_bytes", M, N, K, G), stream)
     ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
     st = _L().bitnet_bitlinear_grouped(x.data_ptr(), _dtype_code(x), M, packed.data_ptr(), w_scale.data_ptr(), N, K,
                                        G, y.data_ptr(), ptr(xq), ptr(sc), ptr(acc), workspace.data_ptr(),

@@ -40,6 +40,8 @@ SIGNATURES = {
     "bitnet_bitlinear_grouped": (_i, [_p, _i, _i64, _p, _p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _sz, _p]),
     "bitnet_bitlinear_swiglu": (_i, [_p, _i, _i64, _p, _p, _p, _p, _i64, _i64, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "bitnet_rmsnorm_quant_act": (_i, [_p, _i, _i64, _i64, _p, _f, _p, _p, _p, _p, _p]),
+    "bitnet_grouped_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64]),
+    "bitnet_w2a8_grouped_ws": (_i, [_p, _p, _i64, _p, _p, _i64, _i64, _i64, _p, _p, _p, _sz, _p]),
     "bitnet_bitlinear_rmsnorm": (_i, [_p, _i, _i64, _p, _f, _p, _p, _i64, _i64, _p, _p, _p, _p, _p, _p, _sz, _p]),
 }
 

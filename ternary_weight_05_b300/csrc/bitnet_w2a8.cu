@@ -18,6 +18,7 @@
 #include "gemv.cuh"
 #include "gemv_ldg.cuh"
 #include "gemv_mma.cuh"
+#include "gemv_mma_grouped.cuh"
 #include "gemv_rows.cuh"
 #include "grouped.cuh"
 #include "pack.cuh"
@@ -353,18 +354,46 @@ bitnet_status launch_gemv_rows(const int8_t *x_q, const float *scale, const void
 // K-block-major, 8/16/32/64 token rows), then the stream-K mma.sync kernel.
 // With x_q == nullptr the prepared activations are already in the workspace
 // (the fused BitLinear prologue wrote them).
+// Group-scaled form of the tensor-core GEMV: the group scales [N, NG], the
+// optional exact per-group products, and where the prep kernel writes the
+// per-token group sums of x_q (in the workspace, after the GEMV's layout).
+struct GroupedArgs {
+  const float *gscale;
+  int32_t *acc_g;
+  int64_t G;
+  int32_t *xsumg;
+};
+
+// Group sizes the grouped tensor-core GEMV takes: groups inside a 512-K
+// unit (64, 128, 256, 512, or one group of up to 512 per row), at most
+// kPrepMaxGroups groups, and a [64][NG] table of group sums in shared memory.
+bool mma_group_ok(int64_t K, int64_t G) {
+  if (G < 64 || K % G != 0 || 512 % G != 0) return false;
+  const int64_t NG = K / G;
+  return NG <= kPrepMaxGroups && 64 * NG * 4 <= kMmaGroupSumsBytes;
+}
+
+// Workspace of the grouped tensor-core path for tokens processed 64 at a
+// time: the GEMV layout plus the group sums.
+size_t grouped_tc_ws_bytes(int64_t M, int64_t N, int64_t K, int64_t G) {
+  const int64_t Mc = std::min<int64_t>(M, BITNET_GEMV_MAX_M);
+  return plan_gemv(Mc, N, K, 148).ws_bytes + (((size_t)Mc * (size_t)(K / G) * 4 + 255) & ~(size_t)255);
+}
+
 bitnet_status launch_gemv_mma(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
                               const float *w_scale, int64_t N, int64_t K, float *y, int32_t *acc, void *workspace,
-                              const GemvPlan &pl, const DeviceInfo *d, cudaStream_t stream) {
+                              const GemvPlan &pl, const DeviceInfo *d, cudaStream_t stream,
+                              const GroupedArgs *ga = nullptr) {
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   uint32_t *xb = reinterpret_cast<uint32_t *>(ws + pl.ws_prep_xb);
   int32_t *xsum = reinterpret_cast<int32_t *>(ws + pl.ws_prep_sums);
   float *fscale = reinterpret_cast<float *>(ws + pl.ws_prep_sums + (size_t)M * 4);
   const int NT = gemv_mma_rows(M);
   if (x_q) {
+    const PrepGroups grp = ga ? PrepGroups{ga->xsumg, (int)ga->G, (int)(K / ga->G)} : PrepGroups{nullptr, 0, 0};
     bitnet_status st = launch(gemm_prep_kernel, dim3(prep_grid(M, pl)), dim3(256), 0, stream, x_q, scale, w_scale,
                               K, xb, xsum, fscale, M, static_cast<uint4 *>(workspace), (int64_t)(pl.ws_zero_bytes / 16),
-                              NT);
+                              NT, grp);
     if (st) return st;
   }
   CUtensorMap wmap, bmap;
@@ -400,6 +429,20 @@ bitnet_status launch_gemv_mma(const int8_t *x_q, const float *scale, int64_t M, 
     const int grid = (int)std::min<long long>((long long)d->sms * ctas, p.units);
     return launch(kernel, dim3(grid), dim3(kMmaThreads), smem, stream, wmap, bmap, p);
   };
+  if (ga) {
+    const GemvMmaGroups gp{ga->gscale, ga->xsumg, ga->acc_g, (int)ga->G, (int)(K / ga->G), (int)(ga->G / kMmaKB)};
+    auto rung = [&](auto kernel, size_t smem, int ctas) -> bitnet_status {
+      if (set_smem(kernel, smem) != BITNET_OK) return BITNET_ERR_CUDA;
+      const int grid = (int)std::min<long long>((long long)d->sms * ctas, p.units);
+      return launch(kernel, dim3(grid), dim3(kMmaThreads), smem, stream, wmap, bmap, p, gp);
+    };
+    switch (NT) {
+      case 8: return rung(gemv_mma_grouped_kernel<1>, GemvMmaGroupedSmem<1>::bytes + 1024, MmaCfg<1>::ctas);
+      case 16: return rung(gemv_mma_grouped_kernel<2>, GemvMmaGroupedSmem<2>::bytes + 1024, MmaCfg<2>::ctas);
+      case 32: return rung(gemv_mma_grouped_kernel<4>, GemvMmaGroupedSmem<4>::bytes + 1024, MmaCfg<4>::ctas);
+      default: return rung(gemv_mma_grouped_kernel<8>, GemvMmaGroupedSmem<8>::bytes + 1024, MmaCfg<8>::ctas);
+    }
+  }
   switch (NT) {
     case 8: return run(gemv_mma_kernel<1>, GemvMmaSmem<1>::bytes + 1024, MmaCfg<1>::ctas);
     case 16: return run(gemv_mma_kernel<2>, GemvMmaSmem<2>::bytes + 1024, MmaCfg<2>::ctas);
@@ -655,7 +698,7 @@ int bitnet_w2a8_gemm(const int8_t *x_q, const float *scale, int64_t M, const uin
   uint8_t *part = ws + gemm_part_offset(M, K);
   bitnet_status st = launch(gemm_prep_kernel, dim3((unsigned)M + gemm_zero_ctas(sp)), dim3(256), 0, stream, x_q,
                             scale, w_scale, K, xb, xsum, fscale, M, reinterpret_cast<uint4 *>(part),
-                            (int64_t)(sp.part_bytes / 16), 0);
+                            (int64_t)(sp.part_bytes / 16), 0, PrepGroups{nullptr, 0, 0});
   if (st) return st;
   return launch_gemm_tc(xb, xsum, fscale, M, packed, N, K, y, acc, sp, part, d, stream);
 }
@@ -818,9 +861,9 @@ bitnet_status bitlinear_tc(const void *x, bool bf, int64_t M, const uint8_t *pac
     bitnet_status st =
         bf ? launch(fused_prep_kernel<__nv_bfloat16>, pgrid, dim3(256), 0, stream,
                     static_cast<const __nv_bfloat16 *>(x), w_scale, K, xb, xsum, fscale, x_q, scale, M, zero, zero_n16,
-                    trows, norm)
+                    trows, norm, PrepGroups{nullptr, 0, 0})
            : launch(fused_prep_kernel<float>, pgrid, dim3(256), 0, stream, static_cast<const float *>(x), w_scale, K,
-                    xb, xsum, fscale, x_q, scale, M, zero, zero_n16, trows, norm);
+                    xb, xsum, fscale, x_q, scale, M, zero, zero_n16, trows, norm, PrepGroups{nullptr, 0, 0});
     if (st) return st;
     if (M <= BITNET_GEMV_MAX_M)
       return launch_gemv_mma(nullptr, nullptr, M, packed, w_scale, N, K, y, acc, workspace, pl, d, stream);
@@ -952,6 +995,59 @@ namespace {
 bool group_shape_ok(int64_t N, int64_t K, int64_t G) {
   return shape_ok(N, K) && G > 0 && G % 4 == 0 && K % G == 0 && K <= 0x7fffffff && N <= 0x7fffffff;
 }
+
+// The grouped tensor-core path's shape and alignment rules.
+bool grouped_tc_ok(int64_t M, int64_t N, int64_t K, int64_t G, const void *packed, const void *x, const void *x_q) {
+  (void)M;
+  (void)N;
+  return K % 64 == 0 && K >= kStageK && K <= kTensorMaxK && mma_group_ok(K, G) && aligned(packed, 16) &&
+         aligned(x, 16) && aligned(x_q, 16);
+}
+
+// Group-scaled matmul on the tensor cores for M >= 3, 64 tokens at a time
+// (chunks of equal size, each >= 3 tokens): per chunk the prep kernel (the
+// fused one from bf16 / fp32 x, else from int8 x_q) writes the operand
+// layout and the group sums, then the grouped GEMV.
+bitnet_status grouped_tc(const void *x, bool bf, const int8_t *x_q_in, const float *scale_in, int64_t M,
+                         const uint8_t *packed, const float *gscale, int64_t N, int64_t K, int64_t G, float *y,
+                         int8_t *xq_out, float *scale_out, int32_t *acc_g, void *workspace, const DeviceInfo *d,
+                         cudaStream_t stream) {
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  const int64_t NG = K / G;
+  const int64_t chunks = cdiv(M, BITNET_GEMV_MAX_M);
+  for (int64_t c = 0; c < chunks; ++c) {
+    const int64_t m0 = M * c / chunks, Mc = M * (c + 1) / chunks - m0;
+    const GemvPlan pl = plan_gemv(Mc, N, K, d->sms);
+    int32_t *xsumg = reinterpret_cast<int32_t *>(ws + pl.ws_bytes);
+    const GroupedArgs ga{gscale, acc_g ? acc_g + m0 * N * NG : nullptr, G, xsumg};
+    if (x_q_in) {
+      if (bitnet_status st = launch_gemv_mma(x_q_in + m0 * K, scale_in + m0, Mc, packed, gscale, N, K, y + m0 * N,
+                                             nullptr, workspace, pl, d, stream, &ga))
+        return st;
+      continue;
+    }
+    uint32_t *xb = reinterpret_cast<uint32_t *>(ws + pl.ws_prep_xb);
+    int32_t *xsum = reinterpret_cast<int32_t *>(ws + pl.ws_prep_sums);
+    float *fscale = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(xsum) + (size_t)Mc * 4);
+    const PrepGroups grp{xsumg, (int)G, (int)NG};
+    const PrepNorm nonorm{nullptr, -1.0f, nullptr};
+    int8_t *xq_c = xq_out ? xq_out + m0 * K : nullptr;
+    float *s_c = scale_out ? scale_out + m0 : nullptr;
+    const dim3 pgrid(prep_grid(Mc, pl));
+    bitnet_status st =
+        bf ? launch(fused_prep_kernel<__nv_bfloat16>, pgrid, dim3(256), 0, stream,
+                    static_cast<const __nv_bfloat16 *>(x) + m0 * K, gscale, K, xb, xsum, fscale, xq_c, s_c, Mc,
+                    static_cast<uint4 *>(workspace), (int64_t)(pl.ws_zero_bytes / 16), gemv_mma_rows(Mc), nonorm, grp)
+           : launch(fused_prep_kernel<float>, pgrid, dim3(256), 0, stream, static_cast<const float *>(x) + m0 * K,
+                    gscale, K, xb, xsum, fscale, xq_c, s_c, Mc, static_cast<uint4 *>(workspace),
+                    (int64_t)(pl.ws_zero_bytes / 16), gemv_mma_rows(Mc), nonorm, grp);
+    if (st) return st;
+    if (bitnet_status s2 = launch_gemv_mma(nullptr, nullptr, Mc, packed, gscale, N, K, y + m0 * N, nullptr, workspace,
+                                           pl, d, stream, &ga))
+      return s2;
+  }
+  return BITNET_OK;
+}
 }  // namespace
 
 int bitnet_pack_weights_grouped(const void *W, int dtype, int64_t N, int64_t K, int64_t G, float alpha, float eps,
@@ -1018,11 +1114,42 @@ int bitnet_bitlinear_grouped(const void *x, int dtype, int64_t M, const uint8_t 
                : launch_gemv_ldg<float, kLdgGrouped>(nullptr, nullptr, x, x_q, scale, M, packed, w_scale, N, K, y,
                                                      acc_g, d, stream, nullptr, nullptr, nullptr, G);
   }
+  // three or more tokens on the tensor cores when the workspace holds that
+  // path's layout: the fused prep kernel (quantisation, operand layout, group
+  // sums) and the grouped GEMV, 64 tokens at a time
+  if (M >= 3 && grouped_tc_ok(M, N, K, G, packed, x, x_q) && workspace_bytes >= grouped_tc_ws_bytes(M, N, K, G))
+    return grouped_tc(x, dtype == BITNET_BF16, nullptr, nullptr, M, packed, w_scale, N, K, G, y, x_q, scale, acc_g,
+                      workspace, d, stream);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   int8_t *xq_buf = x_q ? x_q : reinterpret_cast<int8_t *>(ws);
   float *s_buf = scale ? scale : reinterpret_cast<float *>(ws + (((size_t)M * (size_t)K + 255) & ~(size_t)255));
   if (int st = bitnet_quant_act(x, dtype, M, K, xq_buf, s_buf, stream)) return st;
   return bitnet_w2a8_grouped(xq_buf, s_buf, M, packed, w_scale, N, K, G, y, acc_g, stream);
+}
+
+size_t bitnet_grouped_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t G) {
+  if (M <= 0 || !group_shape_ok(N, K, G) || M > kMaxElems / K || M > kMaxElems / N) return 0;
+  const size_t base = bitnet_bitlinear_grouped_workspace_bytes(M, K);
+  if (M < 3 || !mma_group_ok(K, G) || K % 64 != 0 || K < kStageK || K > kTensorMaxK) return base;
+  return std::max(base, grouped_tc_ws_bytes(M, N, K, G));
+}
+
+int bitnet_w2a8_grouped_ws(const int8_t *x_q, const float *scale, int64_t M, const uint8_t *packed,
+                           const float *w_scale, int64_t N, int64_t K, int64_t G, float *y, int32_t *acc_g,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!x_q || !scale || !packed || !w_scale || !y) return BITNET_ERR_INVALID_ARG;
+  if (M <= 0 || M > 0x7fffffff || !group_shape_ok(N, K, G) || M > kMaxElems / K || M > kMaxElems / N)
+    return BITNET_ERR_SHAPE;
+  if (!aligned(scale, 4) || !aligned(w_scale, 4) || !aligned(y, 4) || !aligned(acc_g, 4))
+    return BITNET_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < bitnet_grouped_workspace_bytes(M, N, K, G) || !aligned(workspace, 256))
+    return BITNET_ERR_WORKSPACE;
+  DeviceInfo *d;
+  if (bitnet_status s = device_info(&d)) return s;
+  if (M >= 3 && grouped_tc_ok(M, N, K, G, packed, x_q, x_q))
+    return grouped_tc(nullptr, false, x_q, scale, M, packed, w_scale, N, K, G, y, nullptr, nullptr, acc_g, workspace, d,
+                      stream);
+  return bitnet_w2a8_grouped(x_q, scale, M, packed, w_scale, N, K, G, y, acc_g, stream);
 }
 
 // ------------------------------------------- training-time (fake-quant) BitLinear --

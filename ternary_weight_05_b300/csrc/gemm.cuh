@@ -265,6 +265,21 @@ __device__ __forceinline__ void prep_zero_row(uint32_t *xb, int64_t m, int64_t K
   }
 }
 
+// Group sums for the group-scaled GEMV: with xsumg non-null the prep kernels
+// also write xsumg[m][g] = sum of x_q over the token's group g of G weights
+// (NG = K / G <= kPrepMaxGroups), and the output scale is s_m / 127 (the
+// weight scales are per group and applied in the GEMV).
+constexpr int kPrepMaxGroups = 1024;
+struct PrepGroups {
+  int32_t *xsumg;
+  int G, NG;
+};
+
+// Adds a 16-K group's sum into the per-group bins (shared memory).
+__device__ __forceinline__ void prep_bin(const PrepGroups &grp, int *bins, int64_t q, int sum) {
+  if (grp.xsumg && sum) atomicAdd(&bins[(int)((q * 16) / grp.G)], sum);
+}
+
 // x_q int8 [M, K] -> fp16 B matrix [M, K] (per 16-K group, element 2i+h is
 // x[16q + 8h + i] * 4^-e(i), e = {0,1,2,3,4,5,0,1}), per-token sum of x_q and
 // the per-token output scale w_scale * s_m / 127.  One CTA per token (CTAs
@@ -273,7 +288,7 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const int8_t *__restrict
                                                         const float *__restrict__ w_scale, int64_t K,
                                                         uint32_t *__restrict__ xb, int32_t *__restrict__ xsum,
                                                         float *__restrict__ fscale, int64_t M, uint4 *zero,
-                                                        int64_t zero_n16, int T) {
+                                                        int64_t zero_n16, int T, const PrepGroups grp) {
   pdl_launch_dependents();
   pdl_wait_prior_grid();
   const int64_t rows = M > T ? M : T;
@@ -286,6 +301,11 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const int8_t *__restrict
     return;
   }
   __shared__ int red[8];
+  __shared__ int bins[kPrepMaxGroups];
+  if (grp.xsumg) {
+    for (int i = threadIdx.x; i < grp.NG; i += 256) bins[i] = 0;
+    __syncthreads();
+  }
   const int64_t m = blockIdx.x;
   const int8_t *row = xq + m * K;
   int sum = 0;
@@ -293,7 +313,9 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const int8_t *__restrict
     const int4 u = *reinterpret_cast<const int4 *>(row + q * 16);
     int8_t v[16];
     memcpy(v, &u, 16);
-    sum += prep_group(v, prep_out(xb, m, q, K, T));
+    const int s16 = prep_group(v, prep_out(xb, m, q, K, T));
+    prep_bin(grp, bins, q, s16);
+    sum += s16;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -303,8 +325,11 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const int8_t *__restrict
     int t = 0;
     for (int w = 0; w < 8; ++w) t += red[w];
     xsum[m] = t;
-    fscale[m] = __fdiv_rn(__fmul_rn(__ldg(w_scale), __ldg(scale + m)), 127.0f);
+    fscale[m] = grp.xsumg ? __fdiv_rn(__ldg(scale + m), 127.0f)
+                          : __fdiv_rn(__fmul_rn(__ldg(w_scale), __ldg(scale + m)), 127.0f);
   }
+  if (grp.xsumg)
+    for (int i = threadIdx.x; i < grp.NG; i += 256) grp.xsumg[m * grp.NG + i] = bins[i];
 }
 
 // Fused BitLinear prologue for the tensor-core paths: per-token absmax
@@ -327,7 +352,7 @@ __global__ void __launch_bounds__(256)
     fused_prep_kernel(const T *__restrict__ x, const float *__restrict__ w_scale, int64_t K,
                       uint32_t *__restrict__ xb, int32_t *__restrict__ xsum, float *__restrict__ fscale,
                       int8_t *__restrict__ xq_out, float *__restrict__ scale_out, int64_t M, uint4 *zero,
-                      int64_t zero_n16, int TR, const PrepNorm norm) {
+                      int64_t zero_n16, int TR, const PrepNorm norm, const PrepGroups grp) {
   pdl_launch_dependents();
   pdl_wait_prior_grid();
   const int64_t rows = M > TR ? M : TR;
@@ -342,6 +367,9 @@ __global__ void __launch_bounds__(256)
   __shared__ float redf[8];
   __shared__ int red[8];
   __shared__ double redd[8];
+  __shared__ int bins[kPrepMaxGroups];
+  if (grp.xsumg)
+    for (int i = threadIdx.x; i < grp.NG; i += 256) bins[i] = 0;  // ordered by the reductions' barriers below
   const int64_t m = blockIdx.x;
   const T *row = x + m * K;
   const bool rms = norm.eps >= 0.0f;  // a negative eps marks "no RMSNorm"
@@ -377,7 +405,9 @@ __global__ void __launch_bounds__(256)
       memcpy(&u, v, 16);
       *reinterpret_cast<int4 *>(xq_out + m * K + q * 16) = u;
     }
-    sum += prep_group(v, prep_out(xb, m, q, K, TR));
+    const int s16 = prep_group(v, prep_out(xb, m, q, K, TR));
+    prep_bin(grp, bins, q, s16);
+    sum += s16;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -387,9 +417,11 @@ __global__ void __launch_bounds__(256)
     int t = 0;
     for (int w = 0; w < 8; ++w) t += red[w];
     xsum[m] = t;
-    fscale[m] = __fdiv_rn(__fmul_rn(__ldg(w_scale), s), 127.0f);
+    fscale[m] = grp.xsumg ? __fdiv_rn(s, 127.0f) : __fdiv_rn(__fmul_rn(__ldg(w_scale), s), 127.0f);
     if (scale_out) scale_out[m] = s;
   }
+  if (grp.xsumg)
+    for (int i = threadIdx.x; i < grp.NG; i += 256) grp.xsumg[m * grp.NG + i] = bins[i];
 }
 
 // --------------------------------------------------------------- main --

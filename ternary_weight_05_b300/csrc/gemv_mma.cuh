@@ -101,6 +101,45 @@ struct GemvMmaSmem {
   static constexpr int bytes = flags + 16;
 };
 
+// The TMA producer of the tensor-core GEMV kernels (one thread): for every
+// unit of the CTA's range, the 128 x 512-K packed-weight tile and the unit's
+// activation slice into the next ring stage.  The weights are requested
+// before waiting on the previous kernel (they do not depend on it).
+template <int NT8, int kStage, int kBBytes, int kBoxRows>
+__device__ __forceinline__ void mma_producer(const CUtensorMap *wmap, const CUtensorMap *bmap, const GemvMmaParams &p,
+                                             uint8_t *ring, uint64_t *full, uint64_t *empty, volatile int *flags,
+                                             long long g0, long long g1) {
+  constexpr int kTok = NT8 * 8, S = MmaCfg<NT8>::stages;
+  prefetch_tensormap(wmap);
+  prefetch_tensormap(bmap);
+  const uint64_t pol_w = l2_policy_evict_first(), pol_b = l2_policy_evict_last();
+  long long it = 0;
+  bool waited = false;
+  for (long long u = g0; u < g1; ++u, ++it) {
+    const int s = (int)(it % S);
+    if (it >= S && !mbar_wait(&empty[s], (uint32_t)(((it / S) - 1) & 1))) {
+      raise_device_error(kDevErrTimeout);
+      flags[0] = 1;
+    }
+    if (flags[0]) break;
+    const int r = (int)(u / p.NCH), c = (int)(u % p.NCH);
+    uint8_t *st = ring + s * kStage;
+    mbar_arrive_expect_tx(&full[s], 16384 + kBBytes);
+    tma_load_2d(st, wmap, &full[s], c * 128, r * 128, pol_w);
+    if (!waited) {  // the activations come from the previous kernel
+      pdl_wait_prior_grid();
+      waited = true;
+    }
+    // the unit's 8 K-blocks x kTok token rows: one box, two for 64 tokens
+    // (rows past K are zero-filled)
+    for (int b = 0; b < 8 * kTok; b += kBoxRows) tma_load_2d(st + 16384 + b * 128, bmap, &full[s], 0, c * 8 * kTok + b, pol_b);
+  }
+  if (!waited) pdl_wait_prior_grid();
+  if (flags[0]) {  // leave no copy in flight (bounded waits)
+    for (long long j = (it > S ? it - S : 0); j < it; ++j) mbar_wait(&full[j % S], (uint32_t)((j / S) & 1));
+  }
+}
+
 template <int NT8>
 __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap bmap,
@@ -131,39 +170,8 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
   __syncthreads();
 
   if (warp == kMmaWarps) {
-    // ------------------------------------------------------------ producer --
-    if (lane == 0) {
-      prefetch_tensormap(&wmap);
-      prefetch_tensormap(&bmap);
-      const uint64_t pol_w = l2_policy_evict_first(), pol_b = l2_policy_evict_last();
-      long long it = 0;
-      bool waited = false;
-      for (long long u = g0; u < g1; ++u, ++it) {
-        const int s = (int)(it % MmaCfg<NT8>::stages);
-        if (it >= MmaCfg<NT8>::stages && !mbar_wait(&empty[s], (uint32_t)(((it / MmaCfg<NT8>::stages) - 1) & 1))) {
-          raise_device_error(kDevErrTimeout);
-          flags[0] = 1;
-        }
-        if (flags[0]) break;
-        const int r = (int)(u / p.NCH), c = (int)(u % p.NCH);
-        uint8_t *st = smem + L::ring + s * L::kStage;
-        mbar_arrive_expect_tx(&full[s], 16384 + L::kBBytes);
-        tma_load_2d(st, &wmap, &full[s], c * 128, r * 128, pol_w);
-        if (!waited) {  // the activations come from the previous kernel
-          pdl_wait_prior_grid();
-          waited = true;
-        }
-        // the unit's 8 K-blocks x kTok token rows: one box, two for 64 tokens
-        // (rows past K are zero-filled)
-        for (int b = 0; b < 8 * L::kTok; b += L::kBoxRows)
-          tma_load_2d(st + 16384 + b * 128, &bmap, &full[s], 0, c * 8 * L::kTok + b, pol_b);
-      }
-      if (!waited) pdl_wait_prior_grid();
-      if (flags[0]) {  // leave no copy in flight (bounded waits)
-        for (long long j = (it > MmaCfg<NT8>::stages ? it - MmaCfg<NT8>::stages : 0); j < it; ++j)
-          mbar_wait(&full[j % MmaCfg<NT8>::stages], (uint32_t)((j / MmaCfg<NT8>::stages) & 1));
-      }
-    }
+    if (lane == 0)
+      mma_producer<NT8, L::kStage, L::kBBytes, L::kBoxRows>(&wmap, &bmap, p, smem + L::ring, full, empty, flags, g0, g1);
     return;
   }
 

@@ -121,6 +121,24 @@ def test_bitlinear_validation(clib):
     assert call(work=FAKE + 16) == WORKSPACE  # not 256-byte aligned
 
 
+def test_grouped_ws_validation(clib):
+    nb = clib.bitnet_grouped_workspace_bytes(16, 300, 2560, 128)
+    assert nb >= clib.bitnet_bitlinear_grouped_workspace_bytes(16, 2560) and nb > 0
+    assert clib.bitnet_grouped_workspace_bytes(16, 300, 2560, 100) == 0  # G does not divide K
+
+    def call(xq=FAKE, M=16, N=300, K=2560, G=128, y=FAKE, work=FAKE, wb=nb):
+        return clib.bitnet_w2a8_grouped_ws(xq, FAKE, M, FAKE, FAKE, N, K, G, y, None, work, wb, None)
+
+    assert call(xq=None) == INVALID_ARG
+    assert call(y=None) == INVALID_ARG
+    assert call(M=0) == SHAPE
+    assert call(G=100) == SHAPE
+    assert call(y=FAKE + 2) == ALIGNMENT
+    assert call(work=None) == WORKSPACE
+    assert call(wb=nb - 1) == WORKSPACE
+    assert call(work=FAKE + 64) == WORKSPACE
+
+
 def test_rmsnorm_validation(clib):
     def quant(x=FAKE, dt=1, M=1, K=64, g=None, eps=2.0 ** -23, xq=FAKE, s=FAKE, h=None):
         return clib.bitnet_rmsnorm_quant_act(x, dt, M, K, g, eps, xq, s, h, None, None)
@@ -327,6 +345,8 @@ def test_injected_cuda_failure_reaches_every_caller(clib):
         "fake_quant": lambda: clib.bitnet_bitlinear_fake_quant(FAKE, 0, FAKE, 1, 2, 8, 64, 1.0, 1e-8, None, FAKE,
                                                                None, None, None, None, None, FAKE, nb_fq, None),
         "selftest": lambda: clib.bitnet_selftest_wait_timeout(2_000_000, None),
+        "w2a8_grouped_ws": lambda: clib.bitnet_w2a8_grouped_ws(FAKE, FAKE, 4, FAKE, FAKE, 8, 512, 128, FAKE, None,
+                                                               FAKE, 1 << 22, None),
         "rmsnorm_quant": lambda: clib.bitnet_rmsnorm_quant_act(FAKE, 1, 2, 64, None, 2.0 ** -23, FAKE, FAKE, None,
                                                                None, None),
         "bitlinear_rmsnorm": lambda: clib.bitnet_bitlinear_rmsnorm(FAKE, 1, 2, FAKE, 2.0 ** -23, FAKE, FAKE, 8, 64,

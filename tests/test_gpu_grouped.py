@@ -7,9 +7,11 @@ scales and per-group int32 products; y is compared with the bound of its
 fp32 arithmetic: y = fl(F * fl(s / 127)) where F adds K/G group terms
 acc_g * scale_g with one rounding per term and per addition (at most K/G + 5
 roundings on the streaming path: J <= 4 terms per lane and 5 shuffle
-additions; K/G on the generic path), each at most 2^-24 of the running sum of
-magnitudes, so |y - y_exact| <= (K/G + 8) * 2^-24 * cond with cond =
-(s / 127) * sum_g |acc_g * scale_g| (computed by the oracle).
+additions; K/G on the generic path; K/G fused multiply-adds plus at most a
+few fp32 atomic additions of split row tiles on the tensor-core path), each
+at most 2^-24 of the running sum of magnitudes, so |y - y_exact| <=
+(K/G + 8) * 2^-24 * cond with cond = (s / 127) * sum_g |acc_g * scale_g|
+(computed by the oracle).
 """
 import numpy as np
 import pytest
@@ -183,3 +185,45 @@ def test_grouped_graph_pdl(lib, oracle_mod, cuda_dev):
         y_ref, cond, _, _, _ = oracle_mod.bitlinear_grouped(e["xf"], p_ref, ws_ref, N, K, G, threads=8)
         assert_grouped_close(e["y"].cpu().numpy(), y_ref, cond, K // G)
     lib.check_device_error()
+
+
+# the tensor-core path (3..64 tokens per chunk, M > 64 in chunks of <= 64):
+# G in {64, 128, 256, 512} or one group per row of <= 512 weights, ragged N
+# across 128-row tiles and split row tiles (stream-K over 512-K units)
+@pytest.mark.parametrize("M", [3, 8, 16, 33, 64, 65, 130])
+@pytest.mark.parametrize("N,K,G", [(300, 2560, 64), (1000, 2560, 128), (129, 8192, 256), (257, 4096, 512),
+                                   (200, 512, 512)])
+def test_w2a8_grouped_tensor_core(lib, oracle_mod, cuda_dev, M, N, K, G):
+    assert lib.grouped_workspace_bytes(M, N, K, G) > lib.bitlinear_grouped_workspace_bytes(M, K)
+    grouped_case(lib, oracle_mod, cuda_dev, M, N, K, G, seed=M * 77 + N + K + G, learned=(M % 2 == 1))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("M", [3, 16, 64, 100])
+def test_bitlinear_grouped_tensor_core(lib, oracle_mod, cuda_dev, dtype, M):
+    """The fused grouped BitLinear on the tensor-core path (the prep kernel
+    quantises, lays out and sums the groups) against the oracle, and bitwise
+    equal to quant_act + the int8 grouped matmul on the same path; a
+    garbage-filled workspace."""
+    import torch
+
+    N, K, G = 700, 2560, 128
+    W = synth.weights_np(N, K, "laplace", 0.01, seed=M + 5)
+    bits, xf = synth.acts_np(M, K, "student_t4", seed=M + 6, outlier_p=0.002, bf16=(dtype == "bf16"))
+    xf[1] = 0.0
+    if bits is not None:
+        bits[1] = 0
+    x = to_dev(bits, cuda_dev, torch.bfloat16) if dtype == "bf16" else to_dev(xf, cuda_dev)
+    packed, ws, _ = lib.pack_weights_grouped(to_dev(W, cuda_dev), G)
+    work = torch.empty(lib.grouped_workspace_bytes(M, N, K, G), dtype=torch.uint8, device=cuda_dev)
+    work.fill_(0xC3)
+    y, acc, xq, s = lib.bitlinear_grouped(x, packed, ws, N, K, G, want_acc=True, want_xq=True, workspace=work)
+    p_ref, ws_ref, _ = oracle_mod.pack_weights_grouped(W, G)
+    y_ref, cond, acc_ref, xq_ref, s_ref = oracle_mod.bitlinear_grouped(xf, p_ref, ws_ref, N, K, G, threads=8)
+    assert np.array_equal(xq.cpu().numpy(), xq_ref) and np.array_equal(s.cpu().numpy(), s_ref)
+    assert np.array_equal(acc.cpu().numpy(), acc_ref)
+    assert_grouped_close(y.cpu().numpy(), y_ref, cond, K // G)
+    y2 = lib.w2a8_grouped(xq, s, packed, ws, N, K, G)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), y2.cpu().numpy().view(np.uint32))
+    lib.check_device_error()
+
