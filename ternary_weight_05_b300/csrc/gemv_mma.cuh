@@ -101,6 +101,34 @@ struct GemvMmaSmem {
   static constexpr int bytes = flags + 16;
 };
 
+// A fragment of 16-K step j (0..3) of a 64-K block from the packed words w0
+// (row g) and w1 (row g + 8) of the lane: each 2-bit field masked in place
+// inside a 16-bit lane is the fp16 value code * 4^i * 2^-24.
+__device__ __forceinline__ void mma_a_frag(uint32_t w0, uint32_t w1, int j, uint32_t &a0, uint32_t &a1, uint32_t &a2,
+                                           uint32_t &a3) {
+  if (j < 3) {
+    const uint32_t m0 = 0x00030003u << (4 * j), m1 = 0x00030003u << (4 * j + 2);
+    a0 = w0 & m0;
+    a1 = w1 & m0;
+    a2 = w0 & m1;
+    a3 = w1 & m1;
+  } else {
+    const uint32_t h0 = w0 >> 12, h1 = w1 >> 12;
+    a0 = h0 & 0x00030003u;
+    a1 = h1 & 0x00030003u;
+    a2 = h0 & 0x000C000Cu;
+    a3 = h1 & 0x000C000Cu;
+  }
+}
+
+// The 16-byte granule ci of token row `tok` of an activation block (rows of
+// 128 bytes, 128-byte swizzle): the B fragments (b0, b1) of 16-K steps
+// 2 (ci % 2) and 2 (ci % 2) + 1 for the lanes with t = ci / 2.  Across a warp
+// (g = token row % 8, t) the eight rows hit eight distinct granule columns.
+__device__ __forceinline__ uint4 mma_b_granule(uint32_t bst, int tok, int ci) {
+  return lds_u128(bst + tok * 128 + (((ci ^ (tok & 7)) & 7) << 4));
+}
+
 // The TMA producer of the tensor-core GEMV kernels (one thread): for every
 // unit of the CTA's range, the 128 x 512-K packed-weight tile and the unit's
 // activation slice into the next ring stage.  The weights are requested
@@ -222,27 +250,20 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
           const uint32_t w1 = lds_u32(st + (r0 + 8) * 128 + off);
           const uint32_t bst = st + 16384 + k2 * L::kTok * 128;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t a0, a1, a2, a3;
-            if (j < 3) {
-              const uint32_t m0 = 0x00030003u << (4 * j), m1 = 0x00030003u << (4 * j + 2);
-              a0 = w0 & m0;
-              a1 = w1 & m0;
-              a2 = w0 & m1;
-              a3 = w1 & m1;
-            } else {
-              const uint32_t h0 = w0 >> 12, h1 = w1 >> 12;
-              a0 = h0 & 0x00030003u;
-              a1 = h1 & 0x00030003u;
-              a2 = h0 & 0x000C000Cu;
-              a3 = h1 & 0x000C000Cu;
-            }
+          for (int jh = 0; jh < 2; ++jh) {
+            // the B fragments of j = 2 jh and 2 jh + 1 sit in one 16-byte
+            // granule per token row: one conflict-free 16-byte load
+            uint4 bq[NT8];
 #pragma unroll
-            for (int nt = 0; nt < NT8; ++nt) {
-              const int tok = nt * 8 + g;
-              const int ci = t * 2 + (j >> 1);
-              const uint2 bv = lds_u64(bst + tok * 128 + (((ci ^ (tok & 7)) & 7) << 4) + ((j & 1) << 3));
-              mma_f16_16816(d[0][nt], a0, a1, a2, a3, bv.x, bv.y);
+            for (int nt = 0; nt < NT8; ++nt) bq[nt] = mma_b_granule(bst, nt * 8 + g, t * 2 + jh);
+#pragma unroll
+            for (int jl = 0; jl < 2; ++jl) {
+              const int j = 2 * jh + jl;
+              uint32_t a0, a1, a2, a3;
+              mma_a_frag(w0, w1, j, a0, a1, a2, a3);
+#pragma unroll
+              for (int nt = 0; nt < NT8; ++nt)
+                mma_f16_16816(d[0][nt], a0, a1, a2, a3, jl ? bq[nt].z : bq[nt].x, jl ? bq[nt].w : bq[nt].y);
             }
           }
         }
@@ -258,34 +279,21 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
         }
         const uint32_t bst = st + 16384 + kb * L::kTok * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t b0[NT8], b1[NT8];
+        for (int jh = 0; jh < 2; ++jh) {
+          uint4 bq[NT8];
 #pragma unroll
-          for (int nt = 0; nt < NT8; ++nt) {
-            const int tok = nt * 8 + g;
-            const int ci = t * 2 + (j >> 1);  // 16-byte chunk of the 128-byte activation row
-            const uint2 bv = lds_u64(bst + tok * 128 + (((ci ^ (tok & 7)) & 7) << 4) + ((j & 1) << 3));
-            b0[nt] = bv.x;
-            b1[nt] = bv.y;
-          }
+          for (int nt = 0; nt < NT8; ++nt) bq[nt] = mma_b_granule(bst, nt * 8 + g, t * 2 + jh);
 #pragma unroll
-          for (int rb = 0; rb < 8; ++rb) {
-            uint32_t a0, a1, a2, a3;
-            if (j < 3) {
-              const uint32_t m0 = 0x00030003u << (4 * j), m1 = 0x00030003u << (4 * j + 2);
-              a0 = w0[rb] & m0;
-              a1 = w1[rb] & m0;
-              a2 = w0[rb] & m1;
-              a3 = w1[rb] & m1;
-            } else {
-              const uint32_t h0 = w0[rb] >> 12, h1 = w1[rb] >> 12;
-              a0 = h0 & 0x00030003u;
-              a1 = h1 & 0x00030003u;
-              a2 = h0 & 0x000C000Cu;
-              a3 = h1 & 0x000C000Cu;
+          for (int jl = 0; jl < 2; ++jl) {
+            const int j = 2 * jh + jl;
+#pragma unroll
+            for (int rb = 0; rb < 8; ++rb) {
+              uint32_t a0, a1, a2, a3;
+              mma_a_frag(w0[rb], w1[rb], j, a0, a1, a2, a3);
+#pragma unroll
+              for (int nt = 0; nt < NT8; ++nt)
+                mma_f16_16816(d[rb][nt], a0, a1, a2, a3, jl ? bq[nt].z : bq[nt].x, jl ? bq[nt].w : bq[nt].y);
             }
-#pragma unroll
-            for (int nt = 0; nt < NT8; ++nt) mma_f16_16816(d[rb][nt], a0, a1, a2, a3, b0[nt], b1[nt]);
           }
         }
       }

@@ -93,11 +93,17 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
   const int64_t NRp = (int64_t)p.NRT * 128;
   float *ws_f = reinterpret_cast<float *>(p.ws_partial);  // split-tile sums F [tokens][NRp]
   const int g = lane >> 2, t = lane & 3;
-  float d[NT8][4], F[NT8][4];
+  // With 64 tokens the running sums F live in the warp's rows of the slice
+  // (registers hold the group accumulators d), else in registers.
+  constexpr bool kFsmem = NT8 == 8;
+  float d[NT8][4], F[NT8][kFsmem ? 1 : 4];
 #pragma unroll
   for (int nt = 0; nt < NT8; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) d[nt][e] = F[nt][e] = 0.0f;
+    for (int e = 0; e < 4; ++e) {
+      d[nt][e] = 0.0f;
+      if (!kFsmem) F[nt][kFsmem ? 0 : e] = 0.0f;
+    }
 
   long long it = 0;
   long long u = g0;
@@ -109,6 +115,12 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
     const int nch = (int)(u_end - u);
     const int row0 = warp * 16 + g;                 // this lane's fragment rows: row0, row0 + 8
     const int64_t n0 = (int64_t)r * 128 + row0, n1 = n0 + 8;
+    if constexpr (kFsmem) {  // this warp's rows of the slice hold F: start from zero
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) fsl[(nt * 8 + 2 * t + (e & 1)) * kMmaRS + row0 + ((e >> 1) << 3)] = 0.0f;
+    }
     for (; u < u_end; ++u, ++it) {
       const int s = (int)(it % MmaCfg<NT8>::stages);
       if (!flags[0] && !mbar_wait(&full[s], (uint32_t)((it / MmaCfg<NT8>::stages) & 1))) {
@@ -131,27 +143,19 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
         const uint32_t w1 = lds_u32(st + (row0 + 8) * 128 + off);
         const uint32_t bst = st + 16384 + k2 * L::kTok * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t a0, a1, a2, a3;
-          if (j < 3) {
-            const uint32_t m0 = 0x00030003u << (4 * j), m1 = 0x00030003u << (4 * j + 2);
-            a0 = w0 & m0;
-            a1 = w1 & m0;
-            a2 = w0 & m1;
-            a3 = w1 & m1;
-          } else {
-            const uint32_t h0 = w0 >> 12, h1 = w1 >> 12;
-            a0 = h0 & 0x00030003u;
-            a1 = h1 & 0x00030003u;
-            a2 = h0 & 0x000C000Cu;
-            a3 = h1 & 0x000C000Cu;
-          }
+        for (int jh = 0; jh < 2; ++jh) {
+          // one conflict-free 16-byte load per token tile holds the B
+          // fragments of 16-K steps 2 jh and 2 jh + 1
+          uint4 bq[NT8];
 #pragma unroll
-          for (int nt = 0; nt < NT8; ++nt) {
-            const int tok = nt * 8 + g;
-            const int ci = t * 2 + (j >> 1);
-            const uint2 bv = lds_u64(bst + tok * 128 + (((ci ^ (tok & 7)) & 7) << 4) + ((j & 1) << 3));
-            mma_f16_16816(d[nt], a0, a1, a2, a3, bv.x, bv.y);
+          for (int nt = 0; nt < NT8; ++nt) bq[nt] = mma_b_granule(bst, nt * 8 + g, t * 2 + jh);
+#pragma unroll
+          for (int jl = 0; jl < 2; ++jl) {
+            uint32_t a0, a1, a2, a3;
+            mma_a_frag(w0, w1, 2 * jh + jl, a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < NT8; ++nt)
+              mma_f16_16816(d[nt], a0, a1, a2, a3, jl ? bq[nt].z : bq[nt].x, jl ? bq[nt].w : bq[nt].y);
           }
         }
         if ((kb + 1) % gp.KBG == 0) {  // the group is complete in d: fold it into F
@@ -165,7 +169,12 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
               const int64_t n = (e >> 1) ? n1 : n0;
               if (tok < p.M && n < p.N) {
                 if (gp.acc_g) gp.acc_g[((int64_t)tok * p.N + n) * gp.NG + grp] = ag;
-                F[nt][e] = __fmaf_rn((float)ag, (e >> 1) ? sc1 : sc0, F[nt][e]);
+                if constexpr (kFsmem) {
+                  float *f = fsl + tok * kMmaRS + row0 + ((e >> 1) << 3);
+                  *f = __fmaf_rn((float)ag, (e >> 1) ? sc1 : sc0, *f);
+                } else {
+                  F[nt][kFsmem ? 0 : e] = __fmaf_rn((float)ag, (e >> 1) ? sc1 : sc0, F[nt][kFsmem ? 0 : e]);
+                }
               }
             }
         }
@@ -175,15 +184,17 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
     }
 
     // ------------------------------------------------------- segment end --
+    if constexpr (!kFsmem) {
 #pragma unroll
-    for (int nt = 0; nt < NT8; ++nt)
+      for (int nt = 0; nt < NT8; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int row = row0 + ((e >> 1) << 3);
-        const int tok = nt * 8 + 2 * t + (e & 1);
-        if (tok < p.M) fsl[tok * kMmaRS + row] = F[nt][e];
-        F[nt][e] = 0.0f;
-      }
+        for (int e = 0; e < 4; ++e) {
+          const int row = row0 + ((e >> 1) << 3);
+          const int tok = nt * 8 + 2 * t + (e & 1);
+          if (tok < p.M) fsl[tok * kMmaRS + row] = F[nt][kFsmem ? 0 : e];
+          F[nt][kFsmem ? 0 : e] = 0.0f;
+        }
+    }
     named_barrier_sync(kMmaBar, kMmaWarps * 32);
     const bool whole = (c0 == 0) && (nch == p.NCH);
     const int entries = 128 * p.M;
