@@ -158,9 +158,10 @@ size_t bitnet_bitlinear_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * call: per-token absmax int8 quantisation of x (§2.2), the ternary integer
  * product and the rescale y = acc * w_scale * s_m / 127 (§2.3).  The
  * quantisation is fused into the matmul's prologue ([Deep-dive] §5.3 names
- * this fusion as a key optimisation): for M <= 2 one kernel, otherwise one
- * kernel that quantises straight into the tensor-core operand layout plus the
- * GEMV (M <= 64) or GEMM kernel.  Results are bit-identical to
+ * this fusion as a key optimisation): for one or two tokens one kernel
+ * (except two tokens with K > 4096 on a matrix of N * K >= 2^27 weights);
+ * otherwise one kernel that quantises straight into the tensor-core operand
+ * layout plus the GEMV (M <= 64) or GEMM kernel.  Results are bit-identical to
  * bitnet_quant_act followed by bitnet_w2a8_gemv / bitnet_w2a8_gemm.
  *
  *   x        device, [M, K] row-major, BITNET_F32 or BITNET_BF16.
@@ -209,8 +210,9 @@ int bitnet_rmsnorm_quant_act(const void *x, int dtype, int64_t M, int64_t K, con
 /*
  * bitnet_bitlinear_rmsnorm -- RMSNorm in front of the BitLinear forward:
  * y = BitLinear(h) with h = RMSNorm(x) formed as bitnet_rmsnorm_quant_act
- * forms it ([Deep-dive] §3.1, §5.3 fusion).  For M >= 3 (K % 64 == 0,
- * 512 <= K <= 65536) one prep kernel computes the RMSNorm, the absmax
+ * forms it ([Deep-dive] §3.1, §5.3 fusion).  For M >= 3, and for two tokens
+ * with K > 4096 and N * K >= 2^27 (K % 64 == 0, 512 <= K <= 65536), one
+ * prep kernel computes the RMSNorm, the absmax
  * quantisation and the tensor-core operand layout, followed by the GEMV
  * (M <= 64) or GEMM kernel; otherwise bitnet_rmsnorm_quant_act runs first,
  * then the int8 GEMV / GEMM.  Results are bit-identical between the two

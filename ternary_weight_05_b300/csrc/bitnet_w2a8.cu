@@ -148,10 +148,10 @@ struct GemvPlan {
   size_t ws_partial_bytes, ws_zero_bytes, ws_prep_xb, ws_prep_sums, ws_bytes;
 };
 
-// Token rows of the prepared activations of the mma.sync GEMV (3..16
-// tokens: padded to 8 or 16, K-block-major); 0 for the other kernels.
+// Token rows of the prepared activations of the mma.sync GEMV (2..64
+// tokens: padded to 8, 16, 32 or 64, K-block-major); 0 for one token.
 int gemv_mma_rows(int64_t M) {
-  if (M < 3 || M > BITNET_GEMV_MAX_M) return 0;
+  if (M < 2 || M > BITNET_GEMV_MAX_M) return 0;
   return M <= 8 ? 8 : (M <= 16 ? 16 : (M <= 32 ? 32 : 64));
 }
 
@@ -309,6 +309,16 @@ bitnet_status launch_gemv_ldg(const int8_t *x_q, const float *scale, const void 
 // The row-range kernel takes one or two tokens whose activation words fit in
 // shared memory beside the weight ring.
 bool rows_ok(int64_t M, int64_t K) { return M <= 2 && M * cdiv(K, kStageK) * kStageK <= kRowsXBudget; }
+// Two tokens whose rows are too long for the streaming kernel's registers
+// (K > 4096) run on the tensor-core GEMV when the matrix is large: its fixed
+// cost is higher (about 12 us against 6.5 us), its cost per byte lower
+// (0.25 against 0.43 us per MB).  Measured: 28672 x 8192 takes 26.4 us
+// against 31.8 us on the row-range kernel, 6912 x 6912 14.9 us against 11.6.
+constexpr int64_t kTwoOnTcMinWeights = (int64_t)1 << 27;  // N * K, about 32 MB packed
+bool two_on_tc(int64_t M, int64_t N, int64_t K, const void *packed) {
+  return M == 2 && N * K >= kTwoOnTcMinWeights && !ldg_ok(M, K, packed) && K % 64 == 0 && K >= kStageK &&
+         K <= kTensorMaxK && aligned(packed, 16);
+}
 
 // Row-range decode GEMV (M <= 2).  XT = int8_t: x_q and scale given;
 // XT = float / bf16: fused form, x quantised in the kernel prologue (x_q and
@@ -638,10 +648,11 @@ int bitnet_w2a8_gemv(const int8_t *x_q, const float *scale, int64_t M, const uin
   }
   if (ldg_ok(M, K, packed) && aligned(x_q, 16))  // one or two tokens, rows up to 8192 / 4096
     return launch_gemv_ldg<int8_t>(x_q, scale, nullptr, nullptr, nullptr, M, packed, w_scale, N, K, y, acc, d, stream);
-  if (rows_ok(M, K))  // one or two tokens: row-range kernel, whole K per CTA, no workspace use
+  if (rows_ok(M, K) && !(two_on_tc(M, N, K, packed) && aligned(x_q, 16)))
+    // one or two tokens: row-range kernel, whole K per CTA, no workspace use
     return launch_gemv_rows<int8_t>(x_q, scale, nullptr, nullptr, nullptr, M, packed, w_scale, N, K, y, acc, d,
                                     stream);
-  if (M >= 3 && K <= kTensorMaxK && aligned(x_q, 16))
+  if (M >= 2 && K <= kTensorMaxK && aligned(x_q, 16))
     return launch_gemv_mma(x_q, scale, M, packed, w_scale, N, K, y, acc, workspace, pl, d, stream);
   CUtensorMap map;
   if (bitnet_status s = encode_packed_map(&map, packed, N, K, kStageRowBytes, kStageRows,
@@ -806,7 +817,7 @@ int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed,
                                                stream)
               : launch_gemv_ldg<float>(nullptr, nullptr, x, x_q, scale, M, packed, w_scale, N, K, y, acc, d, stream);
   }
-  if (fused && rows_ok(M, K)) {
+  if (fused && rows_ok(M, K) && !two_on_tc(M, N, K, packed)) {
     return bf ? launch_gemv_rows<__nv_bfloat16>(nullptr, nullptr, x, x_q, scale, M, packed, w_scale, N, K, y, acc, d,
                                                 stream)
               : launch_gemv_rows<float>(nullptr, nullptr, x, x_q, scale, M, packed, w_scale, N, K, y, acc, d, stream);
@@ -911,7 +922,8 @@ int bitnet_bitlinear_rmsnorm(const void *x, int dtype, int64_t M, const float *g
   const bool bf = dtype == BITNET_BF16;
   // M >= 3 on the tensor cores: the RMSNorm, the quantisation and the
   // operand layout in one prep kernel, then the GEMV / GEMM
-  if (M >= 3 && K % 64 == 0 && K >= kStageK && K <= kTensorMaxK && aligned(packed, 16) && aligned(x_q, 16))
+  if ((M >= 3 || two_on_tc(M, N, K, packed)) && K % 64 == 0 && K >= kStageK && K <= kTensorMaxK &&
+      aligned(packed, 16) && aligned(x_q, 16))
     return bitlinear_tc(x, bf, M, packed, w_scale, N, K, y, x_q, scale, acc, workspace, workspace_bytes, d,
                         PrepNorm{g, eps, ms}, stream);
   // otherwise: RMSNorm + quantisation into int8 (the caller's buffers or the

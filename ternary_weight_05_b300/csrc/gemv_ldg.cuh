@@ -432,25 +432,31 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
 #pragma unroll
     for (int j = 0; j < J; ++j) {
       const int c = lane + 32 * j;
+      // the four rows' chunks first (rows past the stage's end read as zero),
+      // then each field of each word for all four rows in turn, so that
+      // consecutive dp4a feed different accumulators
+      uint32_t wv[kLdgBatch][4];
 #pragma unroll
       for (int r = 0; r < kLdgBatch; ++r) {
-        if (b + r >= nr) continue;  // warp-uniform: the stage's last batch may be short
         uint4 wq = make_uint4(0u, 0u, 0u, 0u);
-        if (c < p.C) wq = lds_u128(smem_u32(stage + (size_t)(b + r) * rowb + (size_t)c * 16));
-        const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t f0 = wv[u] & 0x03030303u, f1 = wv[u] & 0x0C0C0C0Cu;
-          const uint32_t f2 = wv[u] & 0x30303030u, f3 = wv[u] & 0xC0C0C0C0u;
-#pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            a[r][m][0] = dp4a_u8s8(f0, xr[m][j][4 * u + 0], a[r][m][0]);
-            a[r][m][1] = dp4a_u8s8(f1, xr[m][j][4 * u + 1], a[r][m][1]);
-            a[r][m][2] = dp4a_u8s8(f2, xr[m][j][4 * u + 2], a[r][m][2]);
-            a[r][m][3] = dp4a_u8s8(f3, xr[m][j][4 * u + 3], a[r][m][3]);
-          }
-        }
+        if (b + r < nr && c < p.C) wq = lds_u128(smem_u32(stage + (size_t)(b + r) * rowb + (size_t)c * 16));
+        wv[r][0] = wq.x;
+        wv[r][1] = wq.y;
+        wv[r][2] = wq.z;
+        wv[r][3] = wq.w;
       }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int sf = 0; sf < 4; ++sf) {
+          uint32_t f[kLdgBatch];
+#pragma unroll
+          for (int r = 0; r < kLdgBatch; ++r) f[r] = wv[r][u] & (0x03030303u << (2 * sf));
+#pragma unroll
+          for (int r = 0; r < kLdgBatch; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) a[r][m][sf] = dp4a_u8s8(f[r], xr[m][j][4 * u + sf], a[r][m][sf]);
+        }
     }
     const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0;
     const int g = (lane >> 3) & 3;

@@ -70,3 +70,13 @@ def test_bitlinear_workspace_reuse_and_outputs_optional(lib, oracle_mod, cuda_de
             y_ref, _, _, _ = oracle_mod.bitlinear(xf, p_ref, b_ref, N, K, threads=8)
             assert_y_close(y.cpu().numpy(), y_ref)
     lib.check_device_error()
+
+
+# Two tokens with rows longer than 4096 on a matrix of at least 2^27 weights
+# run on the tensor-core GEMV instead of the row-range kernel; N is ragged
+# against the 128-row tile.
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_bitlinear_two_tokens_large_matrix(lib, oracle_mod, cuda_dev, dtype):
+    N, K = 16389, 8192
+    assert N * K >= 1 << 27
+    run_case(lib, oracle_mod, cuda_dev, 2, N, K, dtype, seed=77, zero_row=False)

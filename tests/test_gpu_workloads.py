@@ -6,7 +6,7 @@ outputs the oracle computes row by row (every sampled row for every token):
   2b-decode       q/o 2560^2, gate/up 6912x2560, down 2560x6912  full
   gateup-sweep    13824x2560, M in {1,2,4,8,16,32,64}            full
   prefill-2048    M=2048 x (6912x2560, 2560x6912)                256 sampled rows
-  100b-stream     30 x (28672x8192), M in {1,16}                 pack of layers 0/29
+  100b-stream     30 x (28672x8192), M in {1,2,16}               pack of layers 0/29
                                                                  byte-exact, beta of
                                                                  all 30, 256 rows
   ffn-2b-decode   gate+up 13824x2560 -> SwiGLU -> down 2560x6912 full (graph, PDL)
@@ -110,12 +110,18 @@ def test_100b_stream(lib, oracle_mod, cuda_dev):
         if li not in (0, 29):
             continue
         assert np.array_equal(packed.cpu().numpy().ravel(), p_ref), li
-        for M in (1, 16):
+        # M = 2 on this matrix runs on the tensor-core GEMV (two tokens, long
+        # rows, a large matrix); the fused BitLinear must give the same bits
+        for M in (1, 2, 16):
             bits, xf = synth.acts_np(M, L.K, L.x_dist, seed=L.x_seed)
-            xq, s = lib.quant_act(to_dev(bits, cuda_dev, torch.bfloat16))
+            x = to_dev(bits, cuda_dev, torch.bfloat16)
+            xq, s = lib.quant_act(x)
             y, acc = lib.w2a8_gemv(xq, s, packed, beta, L.N, L.K, want_acc=True)
             rows = np.concatenate([rng.choice(L.N, 256, replace=False), [0, L.N - 1]])
             sampled_check(oracle_mod, xq, s, p_ref, float(b_ref), y, acc, L.N, L.K, rows)
+            yf, accf = lib.bitlinear(x, packed, beta, L.N, L.K, want_acc=True)
+            assert np.array_equal(accf.cpu().numpy(), acc.cpu().numpy()), (li, M)
+            assert np.array_equal(yf.cpu().numpy().view(np.uint32), y.cpu().numpy().view(np.uint32)), (li, M)
 
 
 @pytest.mark.parametrize("pdl", [True, False])
