@@ -385,6 +385,7 @@ __global__ void __launch_bounds__(256)
   }
   amax = block_max_256(amax, redf);
   const float s = amax < 1e-8f ? 1e-8f : amax;
+  const float c = quant_factor(s);
   int sum = 0;
   for (int64_t q = threadIdx.x; q < K / 16; q += 256) {
     float f[8], g[8];
@@ -394,11 +395,13 @@ __global__ void __launch_bounds__(256)
       rms_apply8(f, r, norm.g, q * 16);
       rms_apply8(g, r, norm.g, q * 16 + 8);
     }
-    int8_t v[16];
+    int8_t vf[8], vg[8], v[16];
+    quantize_fast(f, s, c, vf);
+    quantize_fast(g, s, c, vg);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      v[i] = quantize_one(f[i], s);
-      v[8 + i] = quantize_one(g[i], s);
+      v[i] = vf[i];
+      v[8 + i] = vg[i];
     }
     if (xq_out) {
       int4 u;

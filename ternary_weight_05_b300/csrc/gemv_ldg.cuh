@@ -9,10 +9,12 @@
 //     of up to two 8 KB shared-memory stages (sized to the rows the warp
 //     owns, so small matrices leave the SM's shared memory free) with 1D bulk
 //     copies (cp.async.bulk): up to 192 KB in flight per SM, no coupling
-//     between warps, no barrier but the warp's own stage barriers.  The first stages are requested
-//     before waiting on the previous kernel, since the weights do not depend
-//     on it.  Lane l reads the 16-byte chunks l, l+32, ... of each row from
-//     the stage (consecutive lanes, consecutive addresses: conflict-free).
+//     between warps, no barrier but the warp's own stage barriers.  The first
+//     stage is requested before waiting on the previous kernel, since the
+//     weights do not depend on it, the others once the warp has read the
+//     activations (a full ring ahead of those reads delays them).  Lane l
+//     reads the 16-byte chunks l, l+32, ... of each row from the stage
+//     (consecutive lanes, consecutive addresses: conflict-free).
 //   * Because a lane always sees the same K chunks, its activation words live
 //     in registers for the whole kernel: for 16-K group q, word s holds bytes
 //     x_q[16q + 4b + s], b = 0..3, so masking a packed word with
@@ -144,7 +146,7 @@ __host__ __device__ inline GemvLdgSmem gemv_ldg_smem_layout(int MT, int C, int R
   L.xsum = L.xw + MT * C * 64;
   L.fscale = L.xsum + 32;
   L.redf = L.fscale + 32;
-  L.bars = L.redf + kLdgWarps * MT * 4 + 16;
+  L.bars = (L.redf + kLdgWarps * MT * 4 + 16 + 15) & ~15;  // mbarriers: 8-byte aligned
   L.xsumg = L.bars + kLdgWarps * kLdgStages * 8;
   L.bytes = L.xsumg + MT * NG * 4;
   return L;
@@ -213,10 +215,18 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
     const uint32_t xb = (uint32_t)((int64_t)p.M * p.K * sizeof(XT));
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(xs), "r"(xb) : "memory");
   }
+  // Only the first stage goes out before the activations are read: a full
+  // ring (192 KB per SM) ahead of them would hold their loads back by the
+  // time it takes HBM to deliver it.  The other stages follow once this
+  // warp's reads of x (x_q) have returned.
   if (lane == 0) {
     policy = l2_policy_evict_first();
-    for (int st = 0; st < nst && st < NS; ++st) issue(st);
+    if (nst > 0) issue(0);
   }
+  auto issue_rest = [&]() {
+    if (lane == 0)
+      for (int st = issued; st < nst && st < NS; ++st) issue(st);
+  };
   if (GR)
     for (int st = 0; st < nst && st < NS; ++st) issue_scales(st);
 
@@ -241,7 +251,7 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
   // (chunks lane + 32 j) are consecutive granules.
   auto xw_group = [&](int m, int q) { return xw + (size_t)m * p.C * 64 + ((size_t)(q & 3) * p.C + (q >> 2)) * 16; };
   {
-    float s[MT];
+    float s[MT], cq[MT];
     // fused forms: each thread quantises 8-element halves of 16-K groups
     // (up to kLdgGroups * 2 of them, kept in registers from the absmax on)
     float f[2 * kLdgGroups][8];
@@ -271,12 +281,14 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
         for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
         if (lane == 0) redf[warp * MT + m] = a;
       }
+      issue_rest();
       __syncthreads();
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
         float a = redf[m];
         for (int ww = 1; ww < kLdgWarps; ++ww) a = fmaxf(a, redf[ww * MT + m]);
         s[m] = a < 1e-8f ? 1e-8f : a;
+        cq[m] = quant_factor(s[m]);
       }
       if (tid < MT) {
         fscale[tid] = GR ? __fdiv_rn(s[tid], 127.0f) : __fdiv_rn(__fmul_rn(__ldg(p.w_scale), s[tid]), 127.0f);
@@ -299,23 +311,25 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
         for (int mm = 0; mm < MT; ++mm)
           if (mm == m) part[mm] += sum;
       }
+      issue_rest();
     } else {
 #pragma unroll
       for (int n = 0; n < 2 * kLdgGroups; ++n) {
         const int i = tid + n * kLdgThreads;
         if (i < MT * groups * 2) {
           const int m = i / (2 * groups), h = i % (2 * groups), q = h >> 1, half = h & 1;
-          float sm = s[0];
+          float sm = s[0], cm = cq[0];
 #pragma unroll
           for (int mm = 1; mm < MT; ++mm)
-            if (mm == m) sm = s[mm];
+            if (mm == m) {
+              sm = s[mm];
+              cm = cq[mm];
+            }
           int8_t v[8];
+          quantize_fast(f[n], sm, cm, v);
           int sum = 0;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            v[e] = quantize_one(f[n][e], sm);
-            sum += v[e];
-          }
+          for (int e = 0; e < 8; ++e) sum += v[e];
           if (blockIdx.x == 0 && p.xq_out) {
             uint2 u;
             memcpy(&u, v, 8);

@@ -231,12 +231,13 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
       if (lane == 0) redf[warp * MT + m] = a;
     }
     rows_sync();
-    float s[MT];
+    float s[MT], cq[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       float a = redf[m];
       for (int w = 1; w < kRowsComputeWarps; ++w) a = fmaxf(a, redf[w * MT + m]);
       s[m] = a < 1e-8f ? 1e-8f : a;
+      cq[m] = quant_factor(s[m]);
     }
     if (tid < MT) {
       fscale[tid] = __fdiv_rn(__fmul_rn(__ldg(p.w_scale), s[tid]), 127.0f);
@@ -252,12 +253,14 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
       if (q < groups) {
         float f[16];
         rows_load16(x + (int64_t)m * p.K + (int64_t)q * 16, f);
-        float sm = s[0];
+        float sm = s[0], cm = cq[0];
 #pragma unroll
         for (int mm = 1; mm < MT; ++mm)
-          if (mm == m) sm = s[mm];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = quantize_one(f[e], sm);
+          if (mm == m) {
+            sm = s[mm];
+            cm = cq[mm];
+          }
+        quantize_fast(f, sm, cm, v);
         if (blockIdx.x == 0 && p.xq_out) {
           int4 u;
           memcpy(&u, v, 16);

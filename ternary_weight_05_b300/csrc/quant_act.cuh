@@ -24,6 +24,41 @@ __device__ __forceinline__ int8_t quantize_one(float v, float s) {
   return static_cast<int8_t>(q);
 }
 
+// The factor c = fl(127 / s) of quantize_fast.
+__device__ __forceinline__ float quant_factor(float s) { return __fdiv_rn(127.0f, s); }
+
+// quantize_one for E elements of a token whose scale s bounds them all
+// (|v| <= s), with c = quant_factor(s), mostly without a division.
+// t = fl(v * c) and the exact r = fl(fl(v / s) * 127) are each within
+// 127 (2^-23 + 2^-48) of 127 v / s (two roundings of relative size <= 2^-24
+// on a value of magnitude <= 127; where a step underflows, an absolute error
+// below 2^-140 instead), so |t - r| < 2^-14.  When t is
+// farther than 2^-14 from every half-integer, t and r lie strictly between
+// the same two half-integers and round to the same integer (no tie, no
+// clamp needed: |r| <= 127).  t is rounded by adding 1.5 * 2^23, which under
+// round-to-nearest-even leaves the nearest integer in the low mantissa bits
+// (|t| < 2^22).  Elements within 2^-14 of a half-integer, and non-finite
+// ones (the comparison fails for NaN), take quantize_one.
+template <int E>
+__device__ __forceinline__ void quantize_fast(const float (&v)[E], float s, float c, int8_t (&q)[E]) {
+  constexpr float kMagic = 12582912.0f;         // 1.5 * 2^23
+  constexpr float kEdge = 0.5f - 0.00006103515625f;  // 0.5 - 2^-14
+  unsigned slow = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const float t = __fmul_rn(v[e], c);
+    const float a = __fadd_rn(t, kMagic);
+    q[e] = static_cast<int8_t>(__float_as_int(a) - __float_as_int(kMagic));
+    const float d = fabsf(__fsub_rn(t, __fsub_rn(a, kMagic)));
+    if (!(d < kEdge)) slow |= 1u << e;
+  }
+  if (slow) {
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (slow & (1u << e)) q[e] = quantize_one(v[e], s);
+  }
+}
+
 __device__ __forceinline__ float block_max_256(float v, float *red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -54,13 +89,16 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
   }
 }
 
-// Packs the int8 codes of 8 elements into two words.
-__device__ __forceinline__ uint2 quantize8(const float (&v)[8], float s) {
+// Packs the int8 codes of 8 elements of a token (scale s, c = quant_factor(s))
+// into two words.
+__device__ __forceinline__ uint2 quantize8(const float (&v)[8], float s, float c) {
+  int8_t q[8];
+  quantize_fast(v, s, c, q);
   uint32_t lo = 0, hi = 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) lo |= (uint32_t)(uint8_t)quantize_one(v[i], s) << (8 * i);
+  for (int i = 0; i < 4; ++i) lo |= (uint32_t)(uint8_t)q[i] << (8 * i);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) hi |= (uint32_t)(uint8_t)quantize_one(v[4 + i], s) << (8 * i);
+  for (int i = 0; i < 4; ++i) hi |= (uint32_t)(uint8_t)q[4 + i] << (8 * i);
   return make_uint2(lo, hi);
 }
 
@@ -99,11 +137,12 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const T *__res
       for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[r][i]));
     amax = block_max_256(amax, red);
     const float s = amax < 1e-8f ? 1e-8f : amax;
+    const float c = quant_factor(s);
     if (threadIdx.x == 0) scale[m] = s;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int64_t k = ((int64_t)threadIdx.x + (int64_t)r * kQuantThreads) * 8;
-      if (k < K) *reinterpret_cast<uint2 *>(qrow + k) = quantize8(v[r], s);
+      if (k < K) *reinterpret_cast<uint2 *>(qrow + k) = quantize8(v[r], s, c);
     }
     return;
   }
@@ -122,10 +161,11 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_kernel(const T *__res
   if (threadIdx.x == 0) scale[m] = s;
 
   if (VEC) {
+    const float c = quant_factor(s);
     for (int64_t k = (int64_t)threadIdx.x * 8; k < K; k += kQuantThreads * 8) {
       float v[8];
       load8(row + k, v);
-      *reinterpret_cast<uint2 *>(qrow + k) = quantize8(v, s);
+      *reinterpret_cast<uint2 *>(qrow + k) = quantize8(v, s, c);
     }
   } else {
     for (int64_t k = threadIdx.x; k < K; k += kQuantThreads) qrow[k] = quantize_one(load_as_f32(row, k), s);

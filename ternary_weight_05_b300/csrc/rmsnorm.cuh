@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(256) rmsnorm_quant_kernel(const T *__restrict_
   amax = block_max_256(amax, red);
   const float s = amax < 1e-8f ? 1e-8f : amax;
   if (threadIdx.x == 0) scale[m] = s;
+  const float c = quant_factor(s);
   for (int64_t k = (int64_t)threadIdx.x * 8; k < K; k += 256 * 8) {
     float v[8];
     load8(row + k, v);
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(256) rmsnorm_quant_kernel(const T *__restrict_
       hp[0] = make_float4(v[0], v[1], v[2], v[3]);
       hp[1] = make_float4(v[4], v[5], v[6], v[7]);
     }
-    *reinterpret_cast<uint2 *>(xq + m * K + k) = quantize8(v, s);
+    *reinterpret_cast<uint2 *>(xq + m * K + k) = quantize8(v, s, c);
   }
 }
 
