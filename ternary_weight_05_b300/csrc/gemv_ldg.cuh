@@ -171,6 +171,12 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
   const int64_t r0 = (int64_t)(p.N * gw / nw), r1 = (int64_t)(p.N * (gw + 1) / nw);
   const int64_t rowb = p.K / 4;
   const int nst = (int)((r1 - r0 + p.SR - 1) / p.SR);  // this warp's stages
+  // Stage st holds rows [stage_row(st), stage_row(st + 1)): the first stage
+  // takes the remainder (1..SR rows), the others SR each, so that a warp
+  // with one row more than its neighbours requests that row first instead
+  // of waiting a whole round trip for it at the end of the launch.
+  const int first_less = (int)(r1 - r0) - nst * p.SR;  // first stage's rows - SR (<= 0)
+  auto stage_row = [&](int st) -> int64_t { return r0 + max(0, first_less + st * p.SR); };
   uint8_t *ring = lsm + L.ring + (size_t)warp * NS * p.RS;
   uint64_t *wbar = bars + warp * kLdgStages;
   pdl_launch_dependents();
@@ -186,8 +192,8 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
   int issued = 0;  // stages requested (lane 0)
   auto issue = [&](int st) {
     ++issued;
-    const int64_t ra = r0 + (int64_t)st * p.SR;
-    const int64_t rbn = min(ra + p.SR, r1);
+    const int64_t ra = stage_row(st);
+    const int64_t rbn = stage_row(st + 1);
     const uint32_t bytes = (uint32_t)((rbn - ra) * rowb);
     uint64_t *bar = &wbar[st % NS];
     uint8_t *dst = ring + (st % NS) * p.RS;
@@ -200,8 +206,8 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
   int issued_s = 0;
   auto issue_scales = [&](int st) {
     ++issued_s;
-    const int64_t ra = r0 + (int64_t)st * p.SR;
-    const int nr = (int)(min(ra + p.SR, r1) - ra);
+    const int64_t ra = stage_row(st);
+    const int nr = (int)(stage_row(st + 1) - ra);
     float *dst = reinterpret_cast<float *>(ring + (st % NS) * p.RS + (size_t)nr * rowb);
     const float *src = p.w_scale + ra * p.NG;
     for (int e = lane; e < nr * p.NG; e += 32) cp_async4(dst + e, src + e);
@@ -628,8 +634,8 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
       ok = false;  // keep walking (results undefined, the error word says so)
     }
     const uint8_t *stage = ring + slot * p.RS;
-    const int64_t ra = r0 + (int64_t)st * p.SR;
-    const int nr = (int)(min(ra + p.SR, r1) - ra);
+    const int64_t ra = stage_row(st);
+    const int nr = (int)(stage_row(st + 1) - ra);
     if (GR) {
       // this lane's scale copies of the stage are done; then everyone's
       if (issued_s > st + 1) cp_async_wait<1>();
