@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
       for (int n = 0; n < 2 * kLdgGroups; ++n) {
         const int i = tid + n * kLdgThreads;
         if (i < MT * groups * 2) {
-          const int m = i / (2 * groups), h = i % (2 * groups);
+          const int m = MT == 1 ? 0 : i / (2 * groups), h = MT == 1 ? i : i % (2 * groups);
           load8(x + (int64_t)m * p.K + (int64_t)h * 8, f[n]);
           float a = 0.0f;
 #pragma unroll
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
     for (int m = 0; m < MT; ++m) part[m] = 0;
     if constexpr (std::is_same<XT, int8_t>::value) {
       for (int i = tid; i < MT * groups; i += kLdgThreads) {
-        const int m = i / groups, q = i % groups;
+        const int m = MT == 1 ? 0 : i / groups, q = MT == 1 ? i : i % groups;
         int8_t v[16];
         const int4 u = *reinterpret_cast<const int4 *>(p.xq + (int64_t)m * p.K + (int64_t)q * 16);
         memcpy(v, &u, 16);
@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
       for (int n = 0; n < 2 * kLdgGroups; ++n) {
         const int i = tid + n * kLdgThreads;
         if (i < MT * groups * 2) {
-          const int m = i / (2 * groups), h = i % (2 * groups), q = h >> 1, half = h & 1;
+          const int m = MT == 1 ? 0 : i / (2 * groups), h = MT == 1 ? i : i % (2 * groups);
+          const int q = h >> 1, half = h & 1;
           float sm = s[0], cm = cq[0];
 #pragma unroll
           for (int mm = 1; mm < MT; ++mm)
