@@ -177,6 +177,11 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
   // of waiting a whole round trip for it at the end of the launch.
   const int first_less = (int)(r1 - r0) - nst * p.SR;  // first stage's rows - SR (<= 0)
   auto stage_row = [&](int st) -> int64_t { return r0 + max(0, first_less + st * p.SR); };
+  // ring slot of stage st and the parity of its use of that slot (NS is 1 or
+  // 2: no division)
+  static_assert(kLdgStages <= 2, "slot_of / use_of assume at most two stages per warp");
+  auto slot_of = [&](int st) { return NS == 2 ? (st & 1) : 0; };
+  auto use_of = [&](int st) { return (uint32_t)((NS == 2 ? st >> 1 : st) & 1); };
   uint8_t *ring = lsm + L.ring + (size_t)warp * NS * p.RS;
   uint64_t *wbar = bars + warp * kLdgStages;
   pdl_launch_dependents();
@@ -195,8 +200,8 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
     const int64_t ra = stage_row(st);
     const int64_t rbn = stage_row(st + 1);
     const uint32_t bytes = (uint32_t)((rbn - ra) * rowb);
-    uint64_t *bar = &wbar[st % NS];
-    uint8_t *dst = ring + (st % NS) * p.RS;
+    uint64_t *bar = &wbar[slot_of(st)];
+    uint8_t *dst = ring + slot_of(st) * p.RS;
     mbar_arrive_expect_tx(bar, SW ? 2 * bytes : bytes);
     bulk_load(dst, p.packed + ra * rowb, bytes, bar, policy);
     if (SW) bulk_load(dst + bytes, p.packed_up + ra * rowb, bytes, bar, policy);
@@ -208,7 +213,7 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
     ++issued_s;
     const int64_t ra = stage_row(st);
     const int nr = (int)(stage_row(st + 1) - ra);
-    float *dst = reinterpret_cast<float *>(ring + (st % NS) * p.RS + (size_t)nr * rowb);
+    float *dst = reinterpret_cast<float *>(ring + slot_of(st) * p.RS + (size_t)nr * rowb);
     const float *src = p.w_scale + ra * p.NG;
     for (int e = lane; e < nr * p.NG; e += 32) cp_async4(dst + e, src + e);
     cp_async_commit();
@@ -629,8 +634,8 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
   // ------------------------------------------------------------ main loop --
   bool ok = true;
   for (int st = 0; st < nst; ++st) {
-    const int slot = st % NS;
-    if (ok && !mbar_wait(&wbar[slot], (uint32_t)((st / NS) & 1))) {
+    const int slot = slot_of(st);
+    if (ok && !mbar_wait(&wbar[slot], use_of(st))) {
       raise_device_error(kDevErrTimeout);
       ok = false;  // keep walking (results undefined, the error word says so)
     }
@@ -706,7 +711,7 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
   // stages this lane requested last).
   if (!ok && lane == 0) {
     for (int st = (issued > NS ? issued - NS : 0); st < issued; ++st)
-      mbar_wait(&wbar[st % NS], (uint32_t)((st / NS) & 1));
+      mbar_wait(&wbar[slot_of(st)], use_of(st));
   }
   if (GR) cp_async_wait<0>();
 }
