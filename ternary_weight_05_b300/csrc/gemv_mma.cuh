@@ -141,16 +141,20 @@ __device__ __forceinline__ void mma_producer(const CUtensorMap *wmap, const CUte
   prefetch_tensormap(wmap);
   prefetch_tensormap(bmap);
   const uint64_t pol_w = l2_policy_evict_first(), pol_b = l2_policy_evict_last();
-  long long it = 0;
+  int it = 0;  // units this CTA has taken (fewer than 2^31)
   bool waited = false;
+  int r = (int)(g0 / p.NCH), c = (int)(g0 % p.NCH) - 1;  // unit g0 - 1: stepped below
   for (long long u = g0; u < g1; ++u, ++it) {
-    const int s = (int)(it % S);
+    const int s = it % S;
     if (it >= S && !mbar_wait(&empty[s], (uint32_t)(((it / S) - 1) & 1))) {
       raise_device_error(kDevErrTimeout);
       flags[0] = 1;
     }
     if (flags[0]) break;
-    const int r = (int)(u / p.NCH), c = (int)(u % p.NCH);
+    if (++c == p.NCH) {  // (tile, chunk) of unit u
+      c = 0;
+      ++r;
+    }
     uint8_t *st = ring + s * kStage;
     mbar_arrive_expect_tx(&full[s], 16384 + kBBytes);
     tma_load_2d(st, wmap, &full[s], c * 128, r * 128, pol_w);
@@ -164,7 +168,7 @@ __device__ __forceinline__ void mma_producer(const CUtensorMap *wmap, const CUte
   }
   if (!waited) pdl_wait_prior_grid();
   if (flags[0]) {  // leave no copy in flight (bounded waits)
-    for (long long j = (it > S ? it - S : 0); j < it; ++j) mbar_wait(&full[j % S], (uint32_t)((j / S) & 1));
+    for (int j = (it > S ? it - S : 0); j < it; ++j) mbar_wait(&full[j % S], (uint32_t)((j / S) & 1));
   }
 }
 
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
 #pragma unroll
       for (int e = 0; e < 4; ++e) d[rb][nt][e] = 0.0f;
 
-  long long it = 0;
+  int it = 0;  // units this CTA has taken (fewer than 2^31)
   long long u = g0;
   while (u < g1) {
     const int r = (int)(u / p.NCH);
@@ -231,13 +235,14 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
     const long long tile_end = (long long)(r + 1) * p.NCH;
     const long long u_end = tile_end < g1 ? tile_end : g1;  // segment: units [u, u_end) of tile r
     const int nch = (int)(u_end - u);
+    const long long u_seg = u;  // unit u is chunk c0 + (u - u_seg) of tile r
     for (; u < u_end; ++u, ++it) {
       const int s = (int)(it % MmaCfg<NT8>::stages);
       if (!flags[0] && !mbar_wait(&full[s], (uint32_t)((it / MmaCfg<NT8>::stages) & 1))) {
         raise_device_error(kDevErrTimeout);
         flags[0] = 1;
       }
-      const int c = (int)(u % p.NCH);
+      const int c = c0 + (int)(u - u_seg);
       if constexpr (kWide) {
         // row block `warp` over the unit's K-blocks
         const uint32_t st = smem_u32(smem + L::ring + s * L::kStage);

@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
       if (!kFsmem) F[nt][kFsmem ? 0 : e] = 0.0f;
     }
 
-  long long it = 0;
+  int it = 0;  // units this CTA has taken (fewer than 2^31)
   long long u = g0;
   while (u < g1) {
     const int r = (int)(u / p.NCH);
@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
     const long long tile_end = (long long)(r + 1) * p.NCH;
     const long long u_end = tile_end < g1 ? tile_end : g1;
     const int nch = (int)(u_end - u);
+    const long long u_seg = u;  // unit u is chunk c0 + (u - u_seg) of tile r
     const int row0 = warp * 16 + g;                 // this lane's fragment rows: row0, row0 + 8
     const int64_t n0 = (int64_t)r * 128 + row0, n1 = n0 + 8;
     if constexpr (kFsmem) {  // this warp's rows of the slice hold F: start from zero
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(kMmaThreads, MmaCfg<NT8>::ctas)
         raise_device_error(kDevErrTimeout);
         flags[0] = 1;
       }
-      const int c = (int)(u % p.NCH);
+      const int c = c0 + (int)(u - u_seg);
       const uint32_t st = smem_u32(smem + L::ring + s * L::kStage);
       const int nkb = mma_chunk_kbs(p, c);
       float sc0 = 0.0f, sc1 = 0.0f;
