@@ -422,30 +422,51 @@ def run_native(args):
         # end to end through the public API: per pass, the layers' activations
         # from pinned host memory in one copy, one bitlinear call per layer
         # (PDL on, as a user enables it), every output back to pinned host
-        # memory in one copy
+        # memory in one copy.  Two sets of buffers, the copies on their own
+        # streams ordered by events: a pass's readback runs while the next
+        # pass computes, as a serving loop pipelines its tokens.
         xsz = [e["x"].numel() for e in active]
         ysz = [e["y"].numel() for e in active]
         hx = torch.cat([e["x"].reshape(-1) for e in active]).cpu().pin_memory()
-        hy = torch.empty(sum(ysz), dtype=torch.float32).pin_memory()
-        dx = torch.empty_like(hx, device=dev)
-        dy = torch.empty(sum(ysz), dtype=torch.float32, device=dev)
-        xv, yv, ox, oy = [], [], 0, 0
-        for e, nx, ny in zip(active, xsz, ysz):
-            xv.append(dx[ox:ox + nx].view(e["x"].shape))
-            yv.append(dy[oy:oy + ny].view(e["y"].shape))
-            ox += nx
-            oy += ny
+        hy = [torch.empty(sum(ysz), dtype=torch.float32).pin_memory() for _ in range(2)]
+        dx = [torch.empty_like(hx, device=dev) for _ in range(2)]
+        dy = [torch.empty(sum(ysz), dtype=torch.float32, device=dev) for _ in range(2)]
+        xv, yv = [[], []], [[], []]
+        for b in range(2):
+            ox, oy = 0, 0
+            for e, nx, ny in zip(active, xsz, ysz):
+                xv[b].append(dx[b][ox:ox + nx].view(e["x"].shape))
+                yv[b].append(dy[b][oy:oy + ny].view(e["y"].shape))
+                ox += nx
+                oy += ny
         h2d = hx.numel() * hx.element_size()
-        d2h = hy.numel() * hy.element_size()
+        d2h = hy[0].numel() * hy[0].element_size()
+        h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        x_ready = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]  # the pass's kernels: x read, y written
+        y_free = [torch.cuda.Event() for _ in range(2)]
+        n_pass = [0]
 
         def e2e_pass():
-            dx.copy_(hx, non_blocking=True)
-            for e, xd, yd in zip(active, xv, yv):
+            b = n_pass[0] % 2
+            if n_pass[0] >= 2:  # buffer set b was last used two passes ago
+                h2d_stream.wait_event(done[b])
+                stream.wait_event(y_free[b])
+            with torch.cuda.stream(h2d_stream):
+                dx[b].copy_(hx, non_blocking=True)
+                x_ready[b].record(h2d_stream)
+            stream.wait_event(x_ready[b])
+            for e, xd, yd in zip(active, xv[b], yv[b]):
                 if G:
                     tw.bitlinear_grouped(xd, e["packed"], e["beta"], e["n"], e["L"].K, G, out=yd, workspace=ws)
                 else:
                     tw.bitlinear(xd, e["packed"], e["beta"], e["n"], e["L"].K, out=yd, workspace=ws)
-            hy.copy_(dy, non_blocking=True)
+            done[b].record(stream)
+            d2h_stream.wait_event(done[b])
+            with torch.cuda.stream(d2h_stream):
+                hy[b].copy_(dy[b], non_blocking=True)
+                y_free[b].record(d2h_stream)
+            n_pass[0] += 1
 
         for _ in range(2):
             e2e_pass()
