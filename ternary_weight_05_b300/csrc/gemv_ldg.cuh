@@ -166,11 +166,15 @@ __global__ void __launch_bounds__(kLdgThreads, 1) gemv_ldg_kernel(const GemvLdgP
   uint64_t *bars = reinterpret_cast<uint64_t *>(lsm + L.bars);  // [warps][stages]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-  const long long gw = (long long)blockIdx.x * kLdgWarps + warp;
-  const long long nw = (long long)gridDim.x * kLdgWarps;
-  const int64_t r0 = (int64_t)(p.N * gw / nw), r1 = (int64_t)(p.N * (gw + 1) / nw);
+  // rows [N * gw / nw, N * (gw + 1) / nw) of the matrix, formed in 32-bit
+  // arithmetic (N < 2^31, nw <= 2^16): N = qn * nw + rn, so N * gw / nw =
+  // qn * gw + rn * gw / nw with rn * gw < nw^2 < 2^32
+  const unsigned gw = blockIdx.x * kLdgWarps + warp, nw = gridDim.x * kLdgWarps;
+  const unsigned qn = (unsigned)p.N / nw, rn = (unsigned)p.N % nw;
+  const int64_t r0 = (int64_t)qn * gw + rn * gw / nw;
+  const int64_t r1 = (int64_t)qn * (gw + 1) + rn * (gw + 1) / nw;
   const int64_t rowb = p.K / 4;
-  const int nst = (int)((r1 - r0 + p.SR - 1) / p.SR);  // this warp's stages
+  const int nst = ((int)(r1 - r0) + p.SR - 1) / p.SR;  // this warp's stages
   // Stage st holds rows [stage_row(st), stage_row(st + 1)): the first stage
   // takes the remainder (1..SR rows), the others SR each, so that a warp
   // with one row more than its neighbours requests that row first instead
