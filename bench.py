@@ -40,10 +40,12 @@ FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
-# capture of this kernel version (profiles/gemv_ldg_kernel_100b_stream_m1.md,
-# the same 28672 x 8192 launch the default step makes); a step of another
-# shape or another kernel version reports null instead.
-MEASURED_TRAFFIC = {("100b-stream", 1, True, 0): 58.797e6}
+# capture of the current kernel version, keyed by the step's shape; a step of
+# another shape, or a kernel changed since its capture, reports null.  The
+# last capture of the 28672 x 8192 launch (58.797 MB, the algorithmic bytes
+# within 0.1 %: profiles/gemv_ldg_kernel_100b_stream_m1.md) predates the
+# kernel's 32-bit row-range arithmetic, so that shape has no entry.
+MEASURED_TRAFFIC = {}
 
 # Output rows of each prefill matrix the CPU oracle computes per sample pass
 # (all 2048 tokens, the whole K), to keep its timing bounded.
