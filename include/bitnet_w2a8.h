@@ -422,8 +422,9 @@ int bitnet_bitlinear_fake_quant(const void *W, int w_dtype, const void *x, int x
  *   - Sharing: every call, on every stream, uses the same array, and the
  *     array keeps the last call's contents.  Stale contents do not matter:
  *     like bitnet_w2a8_gemv with any workspace, the call zeroes, in stream
- *     order, the part it accumulates into (for M <= 2 the streaming kernels
- *     do not touch the array at all).  Two calls that can overlap on the GPU
+ *     order, the part it accumulates into (the streaming and row-range
+ *     kernels, which take one token and most two-token shapes, do not touch
+ *     the array at all).  Two calls that can overlap on the GPU
  *     (different streams, no ordering between them) race on the array and
  *     give wrong results.  Order them on one stream, or use
  *     bitnet_w2a8_gemv with separate workspaces.

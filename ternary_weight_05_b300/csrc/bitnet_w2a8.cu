@@ -841,7 +841,8 @@ int bitnet_bitlinear(const void *x, int dtype, int64_t M, const uint8_t *packed,
 
 namespace {
 
-// The fused BitLinear on the tensor cores (M >= 3): one prep kernel
+// The fused BitLinear on the tensor cores (M >= 3, and two tokens on a large
+// matrix with long rows): one prep kernel
 // quantises x (after an RMSNorm when norm.eps >= 0) straight into the
 // operand layout, then the GEMV (M <= 64) or the GEMM.
 bitnet_status bitlinear_tc(const void *x, bool bf, int64_t M, const uint8_t *packed, const float *w_scale, int64_t N,
@@ -920,7 +921,8 @@ int bitnet_bitlinear_rmsnorm(const void *x, int dtype, int64_t M, const float *g
   DeviceInfo *d;
   if (bitnet_status s = device_info(&d)) return s;
   const bool bf = dtype == BITNET_BF16;
-  // M >= 3 on the tensor cores: the RMSNorm, the quantisation and the
+  // M >= 3 (and two tokens on a large matrix with long rows) on the tensor
+  // cores: the RMSNorm, the quantisation and the
   // operand layout in one prep kernel, then the GEMV / GEMM
   if ((M >= 3 || two_on_tc(M, N, K, packed)) && K % 64 == 0 && K >= kStageK && K <= kTensorMaxK &&
       aligned(packed, 16) && aligned(x_q, 16))
